@@ -1,0 +1,99 @@
+"""The oracle's pins must catch plausible mistakes (no GPU).
+
+Each case copies kda_oracle.c to a temporary directory, plants one mistake by
+a textual edit (a wrong decay order, a dropped beta, a transposed read-out, a
+missed reset, a wrong tap index, an off-by-one in cu_seqlens ...), compiles
+the copy with gcc and checks that at least one pin from the oracle tests
+fails on it. The oracle itself is never modified.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "kda_oracle.c")
+
+MUTATIONS = {
+    # recurrence
+    "decay_after_update": ("row[j] = row[j] * decay + bk * vt[j];",
+                           "row[j] = (row[j] + bk * vt[j]) * decay;"),
+    "beta_dropped": ("const double bk = bt * kt[i];", "const double bk = kt[i];"),
+    "readout_uses_k": ("acc += S[i * Dv + j] * qt[i];", "acc += S[i * Dv + j] * kt[i];"),
+    "decay_sign": ("const double decay = exp(gt[i]);", "const double decay = exp(-gt[i]);"),
+    "decay_wrong_token": ("const double *gt = J->g + (p * H + h) * Dk;",
+                          "const double *gt = J->g + ((p > 0 ? p - 1 : p) * H + h) * Dk;"),
+    "no_reset_between_docs": ("while (e < T && (seg ? seg[b * T + e] : 1) == s)",
+                              "while (e < T && (seg ? seg[b * T + e] : 1) != 0)"),
+    # conv
+    "conv_tap_forward": ("const int64_t s = t - j;", "const int64_t s = t - (K - 1 - j);"),
+    "conv_no_mask": ("if (seg && seg[b * T + s] != seg[b * T + t])", "if (0)"),
+    # cu_seqlens
+    "cu_off_by_one": ("e = (i < max_segs) ? starts[i] : N;",
+                      "e = (i < max_segs) ? starts[i - 1] : N;"),
+    "cu_padding_starts": ("const int is_start = seg[p] != 0 && (is_row_start || seg[p] != seg[p - 1]);",
+                          "const int is_start = (is_row_start || seg[p] != seg[p - 1]);"),
+}
+
+
+def _build_mutant(tmp_path, name):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new))
+    so = tmp_path / f"lib_{name}.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", str(path),
+                    "-o", str(so), "-lm"], check=True)
+    return str(so)
+
+
+def _pins_pass(monkeypatch, so_path) -> bool:
+    """Run a representative subset of the pins against a mutant library."""
+    lib = ctypes.CDLL(so_path)
+    i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    lib.oracle_cu_seqlens.argtypes = [vp, i64, i64, i32, ctypes.c_int, ctypes.c_int, vp,
+                                      ctypes.POINTER(ctypes.c_int64)]
+    lib.oracle_short_conv.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
+    lib.oracle_kda_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                   ctypes.c_double, vp, ctypes.c_int]
+    monkeypatch.setattr(oracle, "_lib", lib)
+    import tests.test_oracle_cu_seqlens as tc
+    import tests.test_oracle_conv as tv
+    import tests.test_oracle_kda as tk
+    golden = os.path.join(os.path.dirname(tc.__file__), "golden")
+    checks = [
+        lambda: tc.test_worked_examples(golden),
+        lambda: tc.test_matches_cumulative_length_definition("tiny"),
+        lambda: tc.test_bruteforce_two_rows(),
+        lambda: tc.test_overflow_merges_into_last_slot(),
+        lambda: tv.test_no_segments_equals_library_conv1d(4),
+        lambda: tv.test_length_one_document_and_impulse(),
+        lambda: tv.test_packed_equals_concatenated_documents(),
+        lambda: tk.test_closed_form_bruteforce(),
+        lambda: tk.test_hand_worked_three_tokens(),
+        lambda: tk.test_zero_decay_is_causal_linear_attention(),
+        lambda: tk.test_scalar_channel_is_first_order_filter(),
+        lambda: tk.test_length_one_documents(),
+    ]
+    for c in checks:
+        try:
+            c()
+        except AssertionError:
+            return False
+    return True
+
+
+def test_unmodified_copy_passes(tmp_path, monkeypatch):
+    so = tmp_path / "lib_clean.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", SRC, "-o",
+                    str(so), "-lm"], check=True)
+    assert _pins_pass(monkeypatch, str(so))
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutant_is_caught(tmp_path, monkeypatch, name):
+    so = _build_mutant(tmp_path, name)
+    assert not _pins_pass(monkeypatch, so), f"planted mistake '{name}' passed every pin"

@@ -1,0 +1,393 @@
+"""Benchmark of the packed (varlen) KDA forward hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic packed
+input (the Ling3-tiny packed workload by default: B=4, T=8192, H=16,
+D=128, bf16, lognormal documents, max_segs=128):
+    kda_segids_to_cu_seqlens  -> cu_seqlens [max_segs+1]
+    kda_short_conv_varlen x3  -> masked causal conv of the q, k, v projections
+    kda_chunk_fwd_varlen      -> o [B*T, H, D]
+Prints one JSON line. `value` is packed tokens (B*T, padding included) per
+second over the whole job with inputs resident in HBM; `e2e` is the same
+metric through the public API with host buffers (pinned host->device copies
+of the step's inputs and a device->host read of its outputs inside the timed
+region). `roofline` is for the dominant kernel, kda_chunk_fwd_varlen.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+Under torchrun every rank runs its own replica of the workload (rows are
+independent, no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "packed tokens/sec for KDA varlen fwd (1×GB300) and % of roofline"
+UNIT = "tokens/s"
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def maybe_init_dist(ws: int, backend: str):
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(ws: int):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def chunk_bytes_per_token_head(wl: synth.Workload) -> int:
+    """Algorithmic HBM bytes of kda_chunk_fwd_varlen per (token, head): q, k, g
+    (d_qk each), v and o (d_v each) and beta, in the workload dtype."""
+    s = torch.tensor([], dtype=wl.dtype).element_size()
+    return (3 * wl.d_qk + 2 * wl.d_v) * s + s
+
+
+def chunk_flops_per_token_head(wl: synth.Workload) -> int:
+    """The four dense chunk products per token and head at chunk C=64:
+    2*C*(d_qk + d_v) + 4*d_qk*d_v."""
+    C = 64
+    return 2 * C * (wl.d_qk + wl.d_v) + 4 * wl.d_qk * wl.d_v
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [r[0] for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[2]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def make_step_inputs(wl: synth.Workload, device):
+    kin = synth.make_kda_inputs(wl, device=device)
+    cq = synth.make_conv_inputs(wl, seed=synth.default_seed(wl.name) + 101, device=device)
+    ck = synth.make_conv_inputs(wl, seed=synth.default_seed(wl.name) + 102, device=device)
+    cv = synth.make_conv_inputs(wl, seed=synth.default_seed(wl.name) + 103, device=device)
+    return kin, [cq, ck, cv]
+
+
+def run_gb300(args):
+    import kda_segids_cu_gb300 as kda
+
+    ws, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    maybe_init_dist(ws, "nccl")
+    wl = synth.WORKLOADS[args.workload]
+    N, H = wl.N, wl.H
+    kin, convs = make_step_inputs(wl, dev)
+    seg = kin.segment_ids
+    stream = torch.cuda.current_stream()
+
+    # outputs and workspace allocated once (the library allocates nothing)
+    cu = torch.empty(wl.max_segs + 1, dtype=torch.int32, device=dev)
+    nseg = torch.empty(1, dtype=torch.int32, device=dev)
+    ys = [torch.empty_like(c.x) for c in convs]
+    o = torch.empty_like(kin.v)
+    wsb = kda.chunk_fwd_workspace_bytes(wl.B, wl.T, H, wl.d_qk, wl.d_v, wl.dtype)
+    work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ev_chunk = []
+
+    def step(record=False):
+        kda.kda_segids_to_cu_seqlens(seg, wl.max_segs, out=cu, n_segs_out=nseg)
+        for c, y in zip(convs, ys):
+            kda.kda_short_conv_varlen(c.x, c.w, c.segment_ids, out=y)
+        if record:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        kda.kda_chunk_fwd_varlen(kin.q, kin.k, kin.v, kin.g, kin.beta, seg, B=wl.B, T=wl.T,
+                                 out=o, workspace=work, status=status)
+        if record:
+            e1.record(stream)
+            ev_chunk.append((e0, e1))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    ms_local = t0.elapsed_time(t1) / args.steps
+    ms = max_over_ranks(ms_local, ws, dev)
+    chunk_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_chunk)
+    if int(status.item()) != 0:
+        print(f"warning: device status {int(status.item()):#x}", file=sys.stderr)
+
+    # ---- e2e through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        host_in = {"seg": seg.cpu().pin_memory()}
+        for n in ("q", "k", "v", "g", "beta"):
+            host_in[n] = getattr(kin, n).cpu().pin_memory()
+        for i, c in enumerate(convs):
+            host_in[f"x{i}"] = c.x.cpu().pin_memory()
+            host_in[f"w{i}"] = c.w.cpu().pin_memory()
+        host_out = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory()}
+        for i in range(3):
+            host_out[f"y{i}"] = torch.empty(ys[i].shape, dtype=ys[i].dtype).pin_memory()
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+        def e2e_step():
+            for k, v in host_in.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            kda.kda_segids_to_cu_seqlens(dev_in["seg"], wl.max_segs, out=cu, n_segs_out=nseg)
+            for i in range(3):
+                kda.kda_short_conv_varlen(dev_in[f"x{i}"], dev_in[f"w{i}"], dev_in["seg"], out=ys[i])
+            kda.kda_chunk_fwd_varlen(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"],
+                                     dev_in["beta"], dev_in["seg"], B=wl.B, T=wl.T, out=o,
+                                     workspace=work, status=status)
+            host_out["o"].copy_(o, non_blocking=True)
+            for i in range(3):
+                host_out[f"y{i}"].copy_(ys[i], non_blocking=True)
+
+        for _ in range(min(args.warmup, 3)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(ws)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, ws, dev)
+        e2e = {"value": N * ws / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    if rank != 0:
+        return None
+    hbm, tf, tf_sus, peak_src = load_peaks()
+    bytes_launch = chunk_bytes_per_token_head(wl) * N * H
+    flops_launch = chunk_flops_per_token_head(wl) * N * H
+    achieved = bytes_launch / (chunk_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": N * ws / (ms / 1e3),
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; Ling3-tiny packed shape, lognormal EOD-separated documents)",
+        "config": {"workload": f"ling3 packed: B={wl.B} T={wl.T} H={H} D={wl.d_qk} bf16, "
+                               f"max_segs={wl.max_segs}, conv width {wl.k_conv}",
+                   "step": "segids->cu_seqlens + 3 masked short convs + chunked KDA fwd",
+                   "l2": "inputs larger than L2 (chunk inputs 537 MB, conv inputs 403 MB)",
+                   "parallelism": f"replicas x{ws} (rows independent)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None,
+                     "kernel": "kda_chunk_fwd_varlen (planner + chunk kernel)",
+                     "chunk_ms": chunk_ms, "bytes_per_launch": bytes_launch,
+                     "flops_per_launch": flops_launch,
+                     "tensor_frac": flops_launch / (chunk_ms / 1e3) / (tf * 1e12),
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
+        "gpu_launches": args.steps * 6,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, seconds=args.cpu_seconds)
+    else:
+        line["cpu_baseline"] = None
+    return line
+
+
+def cpu_baseline(wl: synth.Workload, seconds: float = 15.0, seed_heads: int | None = None) -> dict:
+    """The fp64 oracle as it stands, on the host cores, on a bounded sample of
+    the workload, scaled to packed tokens/s of the full step."""
+    import oracle
+
+    nt = oracle.default_threads()
+    seg_np, _ = synth.make_segment_ids(wl, synth.default_seed(wl.name))
+    seg = torch.from_numpy(seg_np)
+    # sample: h heads of the recurrence (all tokens), f features of each conv
+    h = seed_heads or wl.H
+    f = 512
+    kin = synth.make_kda_inputs(wl, heads=h)
+    t = time.perf_counter()
+    oracle.cu_seqlens(seg_np, wl.max_segs)
+    t_cu = time.perf_counter() - t
+    ci = synth.make_conv_inputs(wl, features=f)
+    t = time.perf_counter()
+    oracle.short_conv(ci.x, ci.w, ci.segment_ids)
+    t_conv = time.perf_counter() - t
+    t = time.perf_counter()
+    oracle.kda_fwd(kin.q, kin.k, kin.v, kin.g, kin.beta, seg, wl.B, wl.T, n_threads=nt)
+    t_kda = time.perf_counter() - t
+    full = t_cu + 3 * t_conv * (wl.F / f) + t_kda * (wl.H / h)
+    return {"value": wl.N / full, "unit": UNIT, "cores": nt, "kind": "oracle",
+            "sample": f"{wl.name}: cu_seqlens in full; 1 conv on {f} of {wl.F} features "
+                      f"(x3 convs, scaled by features); recurrence on {h} of {wl.H} heads "
+                      f"(all {wl.N} tokens, {nt} threads, scaled by heads); "
+                      f"measured {t_cu + t_conv + t_kda:.1f} s",
+            "seconds_full_step_estimate": full}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return None
+    import oracle
+
+    wl = synth.WORKLOADS[args.workload]
+    nt = oracle.default_threads()
+    seg_np, _ = synth.make_segment_ids(wl, synth.default_seed(wl.name))
+    seg = torch.from_numpy(seg_np)
+    h, f = 1, 128
+    kin = synth.make_kda_inputs(wl, heads=h)
+    ci = synth.make_conv_inputs(wl, features=f)
+
+    def step():
+        t = time.perf_counter()
+        oracle.cu_seqlens(seg_np, wl.max_segs)
+        a = time.perf_counter() - t
+        t = time.perf_counter()
+        oracle.short_conv(ci.x, ci.w, ci.segment_ids)
+        b = time.perf_counter() - t
+        t = time.perf_counter()
+        oracle.kda_fwd(kin.q, kin.k, kin.v, kin.g, kin.beta, seg, wl.B, wl.T, n_threads=nt)
+        c = time.perf_counter() - t
+        return a + 3 * b * (wl.F / f) + c * (wl.H / h)
+
+    for _ in range(args.warmup):
+        step()
+    full = [step() for _ in range(args.steps)]
+    s = statistics.mean(full)
+    value = wl.N / s
+    sample = (f"{wl.name}: per step, cu_seqlens in full, 1 conv on {f} of {wl.F} features "
+              f"(x3, scaled), recurrence on {h} of {wl.H} heads (scaled), {nt} threads")
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "impl": "reference",
+            "config": {"workload": f"ling3 packed: B={wl.B} T={wl.T} H={wl.H} D={wl.d_qk}",
+                       "step": "fp64 CPU oracle: cu_seqlens + 3 masked convs + recurrence"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="ling3", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_gb300(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,165 @@
+/*
+ * kda.h -- C ABI of libkda: the packed (varlen) Kimi Delta Attention forward
+ * on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Sources (web pages):
+ *   [RFC-0025] "RFC-0025: 支持 Attention Varlen 功能并对齐 Loss"
+ *   [RFC-0026] "RFC-0026: Ling3 KDA Varlen 支持（packing 文档间隔离）"
+ *   [Drill]    "Drill: Sequence Packing from scratch"
+ *
+ * Conventions shared by every call
+ *   - Tensor pointers are DEVICE pointers owned by the caller, dense
+ *     (contiguous, row-major) and aligned to 16 bytes. The library never
+ *     frees or retains them.
+ *   - A call validates its arguments on the host, enqueues its kernels on
+ *     `stream` (NULL: the legacy default stream) and returns without
+ *     synchronising. The return value reports argument errors and launch
+ *     errors only; conditions found on the device are written to device
+ *     words the caller reads after its own synchronisation.
+ *   - The library allocates no memory. Scratch space is passed in by the
+ *     caller (see kda_chunk_fwd_varlen_workspace_size).
+ *   - Segment ids are int32 [B, T]: documents carry non-zero ids, 0 marks
+ *     padding. A segment starts where a non-zero id differs from the
+ *     previous token's id, and at t = 0 of every row ([RFC-0026] §3.1.1
+ *     "边界 reset 语义"). The batch is flattened to [1, B*T] ([RFC-0025]
+ *     方案 §2), so tensors indexed by token use the flat index p = b*T + t.
+ *   - Sizes: B*T < 2^31.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL selects the legacy default stream. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1, /* null/misaligned pointer, negative or inconsistent size */
+    KDA_ERR_UNSUPPORTED = -2, /* valid request outside the shapes this build supports   */
+    KDA_ERR_CUDA = -3,        /* a CUDA runtime call or a kernel launch failed          */
+    KDA_ERR_WORKSPACE = -4    /* workspace missing or smaller than required             */
+} kda_status_t;
+
+typedef enum {
+    KDA_F32 = 0, /* IEEE float32 */
+    KDA_BF16 = 1 /* bfloat16     */
+} kda_dtype_t;
+
+/* Bits that kda_chunk_fwd_varlen ORs into *status_dev. */
+#define KDA_DEV_DECAY_RANGE 0x1u /* a chunk's cumulative log-decay left the range
+                                    the chunked factorisation handles (see below) */
+#define KDA_DEV_TIMEOUT 0x2u     /* a bounded in-kernel wait (TMA or tensor-core
+                                    completion) gave up; outputs are incomplete */
+
+/*
+ * kda_segids_to_cu_seqlens -- [RFC-0025] 方案 §1 "segment_ids → cu_seqlens 转换".
+ *
+ * Turns segment ids into cumulative sequence lengths in the FLA convention,
+ * padded to a fixed length: cu_seqlens[0] = 0 and cu_seqlens[i] = end of the
+ * i-th segment of the flattened [B*T] sequence, where a segment ends where
+ * the next one starts ([Drill] 数学: cu[i] = l_1 + ... + l_i). The last real
+ * segment ends one past the last non-padding token; entries past the real
+ * segment count ("phantom" segments) repeat that end, i.e. have zero length.
+ * If the real count exceeds max_segs, cu_seqlens[max_segs] = B*T and the
+ * extra segments merge into the last slot, as on the page; *n_segs_out then
+ * exceeds max_segs, which the caller should treat as an error.
+ *
+ *   segment_ids  device int32 [B, T], 4-byte aligned.
+ *   B, T         B >= 1, T >= 1.
+ *   max_segs     >= 1.
+ *   cu_seqlens   device int32 [max_segs + 1], written entirely.
+ *   n_segs_out   device int32 scalar or NULL: number of real segments.
+ *
+ * Returns KDA_OK, KDA_ERR_INVALID_ARG or KDA_ERR_CUDA. One kernel launch.
+ */
+kda_status_t kda_segids_to_cu_seqlens(const int32_t *segment_ids, int64_t B, int64_t T,
+                                      int32_t max_segs, int32_t *cu_seqlens,
+                                      int32_t *n_segs_out, kda_stream_t stream);
+
+/*
+ * kda_short_conv_varlen -- [RFC-0025] 方案 §3 "ShortConvolution segment 边界 mask".
+ *
+ * Causal depthwise convolution of width k_conv over time, per row:
+ *     y[b,t,f] = sum_{j=0}^{k_conv-1} w[j,f] * x[b,t-j,f]
+ * where a tap contributes only if t-j >= 0 and segment_ids[b,t-j] ==
+ * segment_ids[b,t] (taps that cross a document boundary are zeroed; tap 0
+ * weighs the current token). With segment_ids == NULL only t-j >= 0 is
+ * required. Products are summed in fp32 and rounded once to `dtype`.
+ *
+ *   x, y         device [B, T, F] of `dtype`; y must not overlap x.
+ *   weight       device [k_conv, F] of `dtype`.
+ *   segment_ids  device int32 [B, T] or NULL.
+ *   F            >= 1; F * sizeof(dtype) must be a multiple of 16.
+ *   k_conv       1..8.
+ *
+ * Returns KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED or KDA_ERR_CUDA.
+ */
+kda_status_t kda_short_conv_varlen(const void *x, const void *weight,
+                                   const int32_t *segment_ids, void *y, int64_t B, int64_t T,
+                                   int64_t F, int32_t k_conv, kda_dtype_t dtype,
+                                   kda_stream_t stream);
+
+/*
+ * kda_chunk_fwd_varlen_workspace_size -- bytes of device scratch that
+ * kda_chunk_fwd_varlen needs for these sizes (0 on invalid sizes).
+ */
+size_t kda_chunk_fwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int32_t d_qk,
+                                           int32_t d_v, kda_dtype_t dtype);
+
+/*
+ * kda_chunk_fwd_varlen -- the KDA recurrence over packed sequences,
+ * [RFC-0026] 背景 "KDA 状态泄漏问题" and §3.1.1:
+ *     S'_t = S_{t-1} * exp(g_t)          (g_t in R^{d_qk} scales the key rows)
+ *     S_t  = S'_t + beta_t * k_t v_t^T   (S in R^{d_qk x d_v}, fp32)
+ *     o_t  = scale * S_t^T q_t
+ * with S = 0 at every segment start. Padding tokens contribute nothing and
+ * their output is 0. segment_ids == NULL makes every row one segment.
+ *
+ * Layout: the flattened [1, B*T, H, D] view ([RFC-0025] 方案 §2):
+ *   q, k, g      device [B*T, H, d_qk] of `dtype` (g is the log-decay, <= 0)
+ *   v            device [B*T, H, d_v]  of `dtype`
+ *   beta         device [B*T, H]       of `dtype`
+ *   o            device [B*T, H, d_v]  of `out_dtype` (KDA_F32, or equal to
+ *                `dtype`); values are rounded once, to nearest even, from fp32
+ *   segment_ids  device int32 [B, T] or NULL
+ *
+ * dtype KDA_BF16 runs the chunked form (64-token chunks, tensor cores,
+ * fp32 accumulation and fp32 state); KDA_F32 runs the token recurrence in
+ * fp32 arithmetic. Supported: d_qk == d_v in {64, 128}; H >= 1.
+ *
+ * The chunked form factors the in-chunk decay into per-token scalings
+ * exp(G_i - G_last) and exp(G_last - G_j), G the cumulative log-decay in
+ * the chunk. If some channel's cumulative log-decay over one chunk falls
+ * below -80 (for instance g < -1.25 on every token of a chunk) those factors
+ * leave fp32's range; the kernel then sets KDA_DEV_DECAY_RANGE in
+ * *status_dev and the affected outputs are unreliable.
+ *
+ *   workspace        device scratch of at least
+ *                    kda_chunk_fwd_varlen_workspace_size(...) bytes, 256-byte
+ *                    aligned; its contents on entry do not matter.
+ *   status_dev       device uint32 or NULL; bits are ORed in, never cleared.
+ *
+ * Returns KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE
+ * or KDA_ERR_CUDA. Calls that share a workspace must not overlap in time.
+ */
+kda_status_t kda_chunk_fwd_varlen(const void *q, const void *k, const void *v, const void *g,
+                                  const void *beta, const int32_t *segment_ids, int64_t B,
+                                  int64_t T, int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                  kda_dtype_t dtype, kda_dtype_t out_dtype, void *o, void *workspace,
+                                  size_t workspace_bytes, uint32_t *status_dev,
+                                  kda_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *kda_status_string(kda_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,207 @@
+"""libkda: packed (varlen) Kimi Delta Attention forward for NVIDIA GB300.
+
+A thin ctypes binding over the C ABI in include/kda.h. Every step of the
+computation runs in libkda's CUDA kernels; this module only checks tensor
+properties, allocates outputs and workspace with torch, and passes device
+pointers plus the current CUDA stream. There is no CPU fallback: if
+libkda.so is missing or a call fails, an exception is raised.
+
+Calls (same names as the C ABI):
+  kda_segids_to_cu_seqlens(segment_ids, max_segs) -> (cu_seqlens, n_segs)
+  kda_short_conv_varlen(x, weight, segment_ids=None) -> y
+  kda_chunk_fwd_varlen(q, k, v, g, beta, segment_ids=None, scale=1.0) -> o
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "kda.h")
+
+KDA_OK = 0
+KDA_F32 = 0
+KDA_BF16 = 1
+KDA_DEV_DECAY_RANGE = 0x1
+
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        name = load_library().kda_status_string(status).decode()
+        super().__init__(f"{fn} failed: {name} ({status})")
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libkda.so (built by __graft_entry__.build() or kda_segids_cu_gb300.build)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libkda.so not found at {p}: build it with "
+                           "`python -m kda_segids_cu_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(p)
+    vp, i64, i32, u32p = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_segids_to_cu_seqlens.argtypes = [vp, i64, i64, i32, vp, vp, vp]
+    lib.kda_segids_to_cu_seqlens.restype = ctypes.c_int
+    lib.kda_short_conv_varlen.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_int, vp]
+    lib.kda_short_conv_varlen.restype = ctypes.c_int
+    lib.kda_chunk_fwd_varlen_workspace_size.argtypes = [i64, i64, i32, i32, i32, ctypes.c_int]
+    lib.kda_chunk_fwd_varlen_workspace_size.restype = ctypes.c_size_t
+    lib.kda_chunk_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32,
+                                         ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, vp,
+                                         ctypes.c_size_t, u32p, vp]
+    lib.kda_chunk_fwd_varlen.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def header_functions(header: str = HEADER) -> list[str]:
+    """Names of the functions that include/kda.h declares."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return KDA_BF16
+    if t == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported dtype {t}: libkda takes bfloat16 or float32")
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(fn: str, status: int) -> None:
+    if status != KDA_OK:
+        raise KdaError(fn, status)
+
+
+def kda_segids_to_cu_seqlens(segment_ids: torch.Tensor, max_segs: int, stream=None,
+                             out: torch.Tensor | None = None,
+                             n_segs_out: torch.Tensor | None = None):
+    """[B, T] int32 ids -> (cu_seqlens int32 [max_segs+1], n_segs int32 [1]) on the device."""
+    seg = _dev(segment_ids, "segment_ids")
+    if seg.dtype != torch.int32 or seg.dim() != 2:
+        raise ValueError("segment_ids must be int32 [B, T]")
+    B, T = seg.shape
+    cu = out if out is not None else torch.empty(max_segs + 1, dtype=torch.int32, device=seg.device)
+    n = n_segs_out if n_segs_out is not None else torch.empty(1, dtype=torch.int32, device=seg.device)
+    _check("kda_segids_to_cu_seqlens",
+           load_library().kda_segids_to_cu_seqlens(_ptr(seg), B, T, int(max_segs), _ptr(cu),
+                                                   _ptr(n), _stream_ptr(stream)))
+    return cu, n
+
+
+def kda_short_conv_varlen(x: torch.Tensor, weight: torch.Tensor,
+                          segment_ids: torch.Tensor | None = None, stream=None,
+                          out: torch.Tensor | None = None) -> torch.Tensor:
+    """Segment-masked causal depthwise conv: x [B, T, F], weight [K, F] -> y [B, T, F]."""
+    x = _dev(x, "x")
+    weight = _dev(weight, "weight")
+    if x.dim() != 3 or weight.dim() != 2 or weight.shape[1] != x.shape[2]:
+        raise ValueError("expected x [B, T, F] and weight [K, F]")
+    if weight.dtype != x.dtype:
+        raise ValueError("x and weight must share a dtype")
+    B, T, F = x.shape
+    seg = None
+    if segment_ids is not None:
+        seg = _dev(segment_ids, "segment_ids")
+        if seg.dtype != torch.int32 or tuple(seg.shape) != (B, T):
+            raise ValueError("segment_ids must be int32 [B, T]")
+    y = out if out is not None else torch.empty_like(x)
+    _check("kda_short_conv_varlen",
+           load_library().kda_short_conv_varlen(_ptr(x), _ptr(weight), _ptr(seg), _ptr(y), B, T,
+                                                F, weight.shape[0], _dtype_code(x.dtype),
+                                                _stream_ptr(stream)))
+    return y
+
+
+def chunk_fwd_workspace_bytes(B: int, T: int, H: int, d_qk: int, d_v: int, dtype) -> int:
+    return int(load_library().kda_chunk_fwd_varlen_workspace_size(B, T, H, d_qk, d_v,
+                                                                  _dtype_code(dtype)))
+
+
+def kda_chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                         beta: torch.Tensor, segment_ids: torch.Tensor | None = None,
+                         scale: float = 1.0, B: int | None = None, T: int | None = None,
+                         stream=None, out: torch.Tensor | None = None,
+                         workspace: torch.Tensor | None = None,
+                         status: torch.Tensor | None = None,
+                         out_dtype: torch.dtype | None = None) -> torch.Tensor:
+    """Packed KDA forward. q, k, g: [B, T, H, Dk], [1, B*T, H, Dk] or [B*T, H, Dk];
+    v like q with Dv; beta [..., H]; segment_ids int32 [B, T] or None.
+    Returns o shaped like v, of `out_dtype` (default: the input dtype; float32
+    is also accepted)."""
+    q, k, v, g, beta = (_dev(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (g, "g"),
+                                                 (beta, "beta")))
+    H, Dk = q.shape[-2], q.shape[-1]
+    Dv = v.shape[-1]
+    N = q.numel() // (H * Dk)
+    if segment_ids is not None:
+        seg = _dev(segment_ids, "segment_ids")
+        if seg.dtype != torch.int32 or seg.dim() != 2:
+            raise ValueError("segment_ids must be int32 [B, T]")
+        B, T = seg.shape
+    else:
+        seg = None
+        if B is None or T is None:
+            if q.dim() == 4:
+                B, T = q.shape[0], q.shape[1]
+            else:
+                B, T = 1, N
+    if B * T != N:
+        raise ValueError(f"token count mismatch: B*T = {B * T}, tensors hold {N}")
+    for t, n, d in ((k, "k", Dk), (g, "g", Dk), (v, "v", Dv)):
+        if t.numel() != N * H * d or t.shape[-1] != d or t.dtype != q.dtype:
+            raise ValueError(f"{n} has an unexpected shape or dtype")
+    if beta.numel() != N * H or beta.dtype != q.dtype:
+        raise ValueError("beta must hold B*T*H values of q's dtype")
+    dt = _dtype_code(q.dtype)
+    out_dtype = q.dtype if out_dtype is None else out_dtype
+    if out is not None:
+        out_dtype = out.dtype
+        if out.numel() != v.numel() or not out.is_contiguous():
+            raise ValueError("out must be a contiguous tensor with v's element count")
+    odt = _dtype_code(out_dtype)
+    o = out if out is not None else torch.empty(v.shape, dtype=out_dtype, device=v.device)
+    need = chunk_fwd_workspace_bytes(B, T, H, Dk, Dv, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check("kda_chunk_fwd_varlen",
+           load_library().kda_chunk_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                               _ptr(seg), B, T, H, Dk, Dv, float(scale), dt,
+                                               odt, _ptr(o), _ptr(workspace), workspace.numel(),
+                                               _ptr(status), _stream_ptr(stream)))
+    return o
+
+
+__all__ = ["kda_segids_to_cu_seqlens", "kda_short_conv_varlen", "kda_chunk_fwd_varlen",
+           "chunk_fwd_workspace_bytes", "load_library", "header_functions", "KdaError",
+           "KDA_DEV_DECAY_RANGE"]

@@ -1,0 +1,110 @@
+// kda_api.cu -- libkda's C entry points: host-side validation, then launches
+// on the caller's stream. Semantics and argument contracts are in kda.h.
+#include "kda_common.cuh"
+
+namespace kda {
+size_t recurrent_workspace_bytes(int64_t N);
+size_t tc_workspace_bytes(int64_t N, int32_t H);
+kda_status_t launch_recurrent(const void* q, const void* k, const void* v, const void* g,
+                              const void* beta, const int32_t* seg, int64_t B, int64_t T,
+                              int32_t H, int32_t D, float scale, kda_dtype_t dtype,
+                              kda_dtype_t out_dtype, void* o, void* ws, cudaStream_t stream);
+kda_status_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* g,
+                             const void* beta, const int32_t* seg, int64_t B, int64_t T,
+                             int32_t H, int32_t D, float scale, kda_dtype_t out_dtype, void* o,
+                             void* ws, uint32_t* status_dev, cudaStream_t stream);
+}  // namespace kda
+
+namespace {
+
+constexpr int64_t kMaxTokens = 2147483647LL;   // B*T < 2^31 (int32 token indices)
+
+bool valid_dtype(kda_dtype_t d) { return d == KDA_F32 || d == KDA_BF16; }
+size_t dtype_bytes(kda_dtype_t d) { return d == KDA_BF16 ? 2 : 4; }
+
+bool token_count_ok(int64_t B, int64_t T) {
+    return B >= 1 && T >= 1 && B <= kMaxTokens / T;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(kda_status_t s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+    }
+    return "KDA_UNKNOWN_STATUS";
+}
+
+kda_status_t kda_segids_to_cu_seqlens(const int32_t* segment_ids, int64_t B, int64_t T,
+                                      int32_t max_segs, int32_t* cu_seqlens,
+                                      int32_t* n_segs_out, kda_stream_t stream) {
+    if (!segment_ids || !cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (!token_count_ok(B, T) || max_segs < 1) return KDA_ERR_INVALID_ARG;
+    if (!kda::aligned(segment_ids, 4) || !kda::aligned(cu_seqlens, 4) ||
+        (n_segs_out && !kda::aligned(n_segs_out, 4)))
+        return KDA_ERR_INVALID_ARG;
+    return kda_launch_segids_to_cu_seqlens(segment_ids, B, T, max_segs, cu_seqlens, n_segs_out,
+                                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+kda_status_t kda_short_conv_varlen(const void* x, const void* weight,
+                                   const int32_t* segment_ids, void* y, int64_t B, int64_t T,
+                                   int64_t F, int32_t k_conv, kda_dtype_t dtype,
+                                   kda_stream_t stream) {
+    if (!x || !weight || !y) return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !token_count_ok(B, T) || F < 1) return KDA_ERR_INVALID_ARG;
+    if (k_conv < 1 || k_conv > 8) return KDA_ERR_UNSUPPORTED;
+    if ((F * int64_t(dtype_bytes(dtype))) % 16 != 0) return KDA_ERR_UNSUPPORTED;
+    if (!kda::aligned(x, 16) || !kda::aligned(weight, 16) || !kda::aligned(y, 16) ||
+        (segment_ids && !kda::aligned(segment_ids, 4)))
+        return KDA_ERR_INVALID_ARG;
+    return kda_launch_short_conv(x, weight, segment_ids, y, B, T, F, k_conv, dtype,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t kda_chunk_fwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int32_t d_qk,
+                                           int32_t d_v, kda_dtype_t dtype) {
+    if (!token_count_ok(B, T) || H < 1 || d_qk < 1 || d_v < 1 || !valid_dtype(dtype)) return 0;
+    const int64_t N = B * T;
+    const size_t rec = kda::recurrent_workspace_bytes(N);
+    if (dtype != KDA_BF16) return rec;
+    const size_t tc = kda::tc_workspace_bytes(N, H);
+    return tc > rec ? tc : rec;
+}
+
+kda_status_t kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const int32_t* segment_ids, int64_t B,
+                                  int64_t T, int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                  kda_dtype_t dtype, kda_dtype_t out_dtype, void* o,
+                                  void* workspace, size_t workspace_bytes,
+                                  uint32_t* status_dev, kda_stream_t stream) {
+    if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !valid_dtype(out_dtype) || !token_count_ok(B, T) || H < 1 ||
+        d_qk < 1 || d_v < 1)
+        return KDA_ERR_INVALID_ARG;
+    if (out_dtype != dtype && out_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return KDA_ERR_UNSUPPORTED;
+    if (int64_t(H) * d_qk > 65536) return KDA_ERR_UNSUPPORTED;
+    const void* ptrs[] = {q, k, v, g, beta, o};
+    for (const void* p : ptrs)
+        if (!kda::aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (segment_ids && !kda::aligned(segment_ids, 4)) return KDA_ERR_INVALID_ARG;
+    if (status_dev && !kda::aligned(status_dev, 4)) return KDA_ERR_INVALID_ARG;
+    const size_t need = kda_chunk_fwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
+    if (!workspace || workspace_bytes < need || !kda::aligned(workspace, 256))
+        return KDA_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == KDA_BF16)
+        return kda::launch_chunk_tc(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale,
+                                    out_dtype, o, workspace, status_dev, st);
+    return kda::launch_recurrent(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale, dtype,
+                                 out_dtype, o, workspace, st);
+}
+
+}  // extern "C"

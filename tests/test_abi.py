@@ -1,0 +1,90 @@
+"""The C ABI library loads, exports every function include/kda.h declares,
+and rejects invalid arguments on the host before touching the GPU (no GPU)."""
+import ctypes
+
+import pytest
+
+import kda_segids_cu_gb300 as kda
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return kda.load_library()
+
+
+def test_exports_every_declared_function(lib):
+    names = kda.header_functions()
+    assert {"kda_segids_to_cu_seqlens", "kda_short_conv_varlen", "kda_chunk_fwd_varlen",
+            "kda_chunk_fwd_varlen_workspace_size", "kda_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"libkda.so does not export {n}"
+
+
+def test_status_strings(lib):
+    for code, name in [(0, b"KDA_OK"), (-1, b"KDA_ERR_INVALID_ARG"), (-2, b"KDA_ERR_UNSUPPORTED"),
+                       (-3, b"KDA_ERR_CUDA"), (-4, b"KDA_ERR_WORKSPACE")]:
+        assert lib.kda_status_string(code) == name
+
+
+def test_workspace_size_host_logic(lib):
+    f = lib.kda_chunk_fwd_varlen_workspace_size
+    assert f(4, 8192, 16, 128, 128, kda.KDA_BF16) > 0
+    assert f(1, 256, 2, 64, 64, kda.KDA_F32) > 0
+    assert f(0, 8, 1, 64, 64, kda.KDA_F32) == 0          # invalid sizes
+    assert f(1, 8, 0, 64, 64, kda.KDA_F32) == 0
+    assert f(1 << 20, 1 << 12, 1, 64, 64, kda.KDA_F32) == 0   # B*T >= 2^31
+    assert f(1, 8, 1, 64, 64, 7) == 0                     # unknown dtype
+
+
+FAKE = ctypes.c_void_p(4096)    # aligned, never dereferenced: validation fails first
+ODD = ctypes.c_void_p(4098)
+
+
+def test_segids_rejects_invalid_arguments(lib):
+    f = lib.kda_segids_to_cu_seqlens
+    assert f(None, 1, 4, 4, FAKE, None, None) == -1
+    assert f(FAKE, 1, 4, 4, None, None, None) == -1
+    assert f(FAKE, 0, 4, 4, FAKE, None, None) == -1
+    assert f(FAKE, 1, 0, 4, FAKE, None, None) == -1
+    assert f(FAKE, 1, 4, 0, FAKE, None, None) == -1
+    assert f(ODD, 1, 4, 4, FAKE, None, None) == -1
+    assert f(FAKE, 1 << 20, 1 << 12, 4, FAKE, None, None) == -1
+
+
+def test_conv_rejects_invalid_arguments(lib):
+    f = lib.kda_short_conv_varlen
+    assert f(None, FAKE, None, FAKE, 1, 4, 8, 4, 1, None) == -1
+    assert f(FAKE, FAKE, None, FAKE, 1, 4, 8, 0, 1, None) == -2     # k_conv out of range
+    assert f(FAKE, FAKE, None, FAKE, 1, 4, 8, 9, 1, None) == -2
+    assert f(FAKE, FAKE, None, FAKE, 1, 4, 7, 4, 1, None) == -2     # F*2 not a multiple of 16
+    assert f(ODD, FAKE, None, FAKE, 1, 4, 8, 4, 1, None) == -1      # misaligned
+    assert f(FAKE, FAKE, None, FAKE, 1, 4, 8, 4, 3, None) == -1     # dtype
+
+
+def test_chunk_rejects_invalid_arguments(lib):
+    f = lib.kda_chunk_fwd_varlen
+    ws = lib.kda_chunk_fwd_varlen_workspace_size(1, 64, 2, 64, 64, kda.KDA_BF16)
+    args = [FAKE] * 5 + [None, 1, 64, 2, 64, 64, ctypes.c_float(1.0), kda.KDA_BF16, kda.KDA_BF16,
+                         FAKE, FAKE, ws, None, None]
+
+    def call(**over):
+        a = list(args)
+        idx = {"q": 0, "seg": 5, "B": 6, "H": 8, "dk": 9, "dv": 10, "dtype": 12, "out_dtype": 13,
+               "o": 14, "ws": 15, "ws_bytes": 16, "status": 17}
+        for k, v in over.items():
+            a[idx[k]] = v
+        return f(*a)
+
+    assert call(q=None) == -1
+    assert call(o=None) == -1
+    assert call(q=ODD) == -1
+    assert call(B=0) == -1
+    assert call(dtype=5) == -1
+    assert call(out_dtype=5) == -1
+    assert call(dtype=kda.KDA_F32, out_dtype=kda.KDA_BF16) == -2   # no narrowing output
+    assert call(dk=96, dv=96) == -2
+    assert call(dk=64, dv=128) == -2
+    assert call(ws=None) == -4
+    assert call(ws_bytes=ws - 1) == -4
+    assert call(ws=ctypes.c_void_p(4096 + 16)) == -4          # workspace must be 256-aligned
+    assert call(status=ODD) == -1

@@ -1,0 +1,172 @@
+"""GPU parity and invariants for kda_chunk_fwd_varlen.
+
+Bar (per head, over real tokens): max|o - o_ref| <= 2e-2 RMS(o_ref) for bf16
+inputs, <= 1e-4 RMS(o_ref) for fp32 inputs; padding outputs exactly 0.
+Small workloads are compared in full; the large ones at their full size, in
+the launch configuration the bench times, on sampled heads that the oracle
+computes in seconds. Bit-exact invariants: documents do not leak into each
+other, rows are independent, segment_ids=None equals all-ones ids, reruns are
+deterministic.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kda_segids_cu_gb300 as kda
+import oracle
+import synth
+from tests.parity import check_kda_output
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_fwd(inp, B, T, scale=1.0, seg="inputs", out_dtype=None):
+    s = inp.segment_ids if seg == "inputs" else seg
+    o = kda.kda_chunk_fwd_varlen(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), inp.g.cuda(),
+                                 inp.beta.cuda(), None if s is None else s.cuda(), scale=scale,
+                                 B=B, T=T, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return o
+
+
+def _oracle(inp, B, T, heads=None, scale=1.0, seg="inputs"):
+    s = inp.segment_ids if seg == "inputs" else seg
+    if heads is None:
+        return oracle.kda_fwd(inp.q, inp.k, inp.v, inp.g, inp.beta, s, B, T, scale=scale)
+    hs = torch.tensor(heads)
+    pick = lambda t: t.index_select(1, hs.to(t.device)).cpu()
+    return oracle.kda_fwd(pick(inp.q), pick(inp.k), pick(inp.v), pick(inp.g), pick(inp.beta),
+                          None if s is None else s.cpu(), B, T, scale=scale)
+
+
+@pytest.mark.parametrize("name", ["tiny", "b2"])
+def test_small_workloads_full(name):
+    wl = synth.WORKLOADS[name]
+    inp = synth.make_kda_inputs(wl)
+    ref = _oracle(inp, wl.B, wl.T)
+    # fp32 output: the strict per-head bound; input-dtype output: plus its rounding
+    o32 = _gpu_fwd(inp, wl.B, wl.T, out_dtype=torch.float32)
+    check_kda_output(o32, ref, inp.segment_ids, wl.dtype, label=name + "/f32 out")
+    o = _gpu_fwd(inp, wl.B, wl.T)
+    assert o.dtype == wl.dtype
+    check_kda_output(o, ref, inp.segment_ids, wl.dtype, label=name)
+
+
+@pytest.mark.parametrize("name,heads", [("ling3", [0, 7, 15]), ("short", [0, 15]),
+                                        ("long", [0, 31]), ("long_none", [5])])
+def test_large_workloads_sampled_heads(name, heads):
+    wl = synth.WORKLOADS[name]
+    inp = synth.make_kda_inputs(wl, device="cuda")
+    ref = _oracle(inp, wl.B, wl.T, heads=heads)
+    o = _gpu_fwd(inp, wl.B, wl.T)
+    check_kda_output(o, ref, inp.segment_ids, wl.dtype, heads=heads, label=name)
+    o32 = _gpu_fwd(inp, wl.B, wl.T, out_dtype=torch.float32)
+    check_kda_output(o32, ref, inp.segment_ids, wl.dtype, heads=heads, label=name + "/f32 out")
+    # the bf16 output is the fp32 output rounded once to nearest even
+    assert torch.equal(o, o32.to(wl.dtype))
+
+
+def test_long_none_equals_single_segment():
+    # segment_ids=None on the long workload equals one all-ones segment, bitwise
+    wl = synth.WORKLOADS["long_none"]
+    inp = synth.make_kda_inputs(wl, device="cuda", heads=4)
+    a = _gpu_fwd(inp, wl.B, wl.T)
+    b = _gpu_fwd(inp, wl.B, wl.T, seg=torch.ones(wl.B, wl.T, dtype=torch.int32))
+    assert torch.equal(a, b)
+
+
+def _small_random(B, T, H, D, dtype, seed, max_len=80, pad_prob=0.0, ids="increasing"):
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator().manual_seed(seed)
+    seg = torch.from_numpy(synth.random_segment_ids(rng, B, T, max_len=max_len,
+                                                    pad_prob=pad_prob, ids=ids))
+    N = B * T
+    q = torch.nn.functional.normalize(torch.randn(N, H, D, generator=gen), dim=-1).to(dtype)
+    k = torch.nn.functional.normalize(torch.randn(N, H, D, generator=gen), dim=-1).to(dtype)
+    v = torch.randn(N, H, D, generator=gen).to(dtype)
+    g = (-torch.exp(torch.randn(N, H, D, generator=gen) * 0.5 - 2.0)).to(dtype)
+    beta = torch.sigmoid(torch.randn(N, H, generator=gen)).to(dtype)
+    return synth.KdaInputs(q, k, v, g, beta, seg, [])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("D", [64, 128])
+def test_boundary_sweep(dtype, D):
+    """Ragged T, several chunks, boundaries at every in-chunk offset, length-1
+    documents, interior and leading padding, arbitrary (non-monotone) ids."""
+    cases = [
+        dict(B=1, T=64 * 5 + 17, max_len=70),
+        dict(B=3, T=100, max_len=9, pad_prob=0.25),
+        dict(B=2, T=200, max_len=3, ids="arbitrary"),
+        dict(B=1, T=333, max_len=200, pad_prob=0.1),
+        dict(B=1, T=130, max_len=1),
+    ]
+    for i, c in enumerate(cases):
+        B, T = c.pop("B"), c.pop("T")
+        inp = _small_random(B, T, 2, D, dtype, seed=100 * D + i, **c)
+        o = _gpu_fwd(inp, B, T, scale=0.5)
+        ref = _oracle(inp, B, T, scale=0.5)
+        check_kda_output(o, ref, inp.segment_ids, dtype, label=f"case{i}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_every_boundary_offset(dtype):
+    # one document boundary at each offset 1..64 of the second chunk
+    for off in range(1, 65):
+        T = 192
+        seg = torch.ones(1, T, dtype=torch.int32)
+        seg[0, 64 + off:] = 2
+        inp = _small_random(1, T, 1, 64, dtype, seed=off)
+        inp.segment_ids = seg
+        check_kda_output(_gpu_fwd(inp, 1, T), _oracle(inp, 1, T), seg, dtype, label=f"off{off}")
+
+
+def test_isolation_bitwise():
+    """Changing one document's values leaves every other document's output bitwise
+    unchanged (no state leaks across a boundary)."""
+    wl = synth.WORKLOADS["b2"]
+    inp = synth.make_kda_inputs(wl)
+    o1 = _gpu_fwd(inp, wl.B, wl.T).cpu()
+    seg = inp.segment_ids.reshape(-1)
+    victim = (seg == 3)
+    victim[wl.T:] = False                     # document 3 of row 0
+    inp2 = synth.KdaInputs(inp.q.clone(), inp.k.clone(), inp.v.clone(), inp.g.clone(),
+                           inp.beta.clone(), inp.segment_ids, [])
+    inp2.v[victim] = -inp2.v[victim] * 3
+    inp2.q[victim] = inp2.k[victim]
+    o2 = _gpu_fwd(inp2, wl.B, wl.T).cpu()
+    assert torch.equal(o1[~victim], o2[~victim])
+    assert not torch.equal(o1[victim], o2[victim])
+
+
+def test_row_independence_and_determinism():
+    B, T = 3, 300
+    inp = _small_random(B, T, 2, 128, torch.bfloat16, seed=9, max_len=90)
+    a = _gpu_fwd(inp, B, T).cpu()
+    seg2 = inp.segment_ids.clone()
+    seg2[2] = torch.from_numpy(synth.random_segment_ids(np.random.default_rng(1), 1, T, 20))[0]
+    b = _gpu_fwd(inp, B, T, seg=seg2).cpu()
+    assert torch.equal(a[: 2 * T], b[: 2 * T])
+    c = _gpu_fwd(inp, B, T).cpu()
+    assert torch.equal(a, c)
+
+
+def test_none_equals_all_ones():
+    B, T = 2, 257
+    for dtype in (torch.bfloat16, torch.float32):
+        inp = _small_random(B, T, 2, 64, dtype, seed=3)
+        a = _gpu_fwd(inp, B, T, seg=None)
+        b = _gpu_fwd(inp, B, T, seg=torch.ones(B, T, dtype=torch.int32))
+        assert torch.equal(a, b)
+        check_kda_output(a, _oracle(inp, B, T, seg=None), None, dtype, label="none")
+
+
+def test_all_padding_and_tiny_shapes():
+    for (B, T) in [(1, 1), (1, 63), (2, 65), (5, 3)]:
+        inp = _small_random(B, T, 3, 64, torch.bfloat16, seed=B * 100 + T, max_len=5)
+        check_kda_output(_gpu_fwd(inp, B, T), _oracle(inp, B, T), inp.segment_ids,
+                         torch.bfloat16, label=f"{B}x{T}")
+    inp = _small_random(2, 70, 2, 64, torch.bfloat16, seed=1)
+    zeros = torch.zeros(2, 70, dtype=torch.int32)
+    o = _gpu_fwd(inp, 2, 70, seg=zeros)
+    assert torch.count_nonzero(o).item() == 0

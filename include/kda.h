@@ -155,6 +155,42 @@ kda_status_t kda_chunk_fwd_varlen(const void *q, const void *k, const void *v, c
                                   size_t workspace_bytes, uint32_t *status_dev,
                                   kda_stream_t stream);
 
+/*
+ * kda_chunk_fwd_varlen_noalloc -- kda_chunk_fwd_varlen for callers that cannot
+ * allocate device memory. The pages have no counterpart: this is a calling
+ * convention of this library, not part of the method.
+ *
+ * Some callers hold no device allocator: a plain C host program that only
+ * receives device buffers from another runtime, or a serving loop whose memory
+ * pool owns all free device memory and forbids further cudaMalloc/cudaFree on
+ * its hot path (those calls can also synchronise the device). They cannot hand
+ * kda_chunk_fwd_varlen a workspace, so this entry point takes its scratch from
+ * an array compiled into the library instead: KDA_NOALLOC_SCRATCH_BYTES bytes of
+ * device memory that every GPU loading the library holds until the process
+ * exits. It allocates nothing and calls no allocating routine.
+ *
+ * Arguments, layouts and results are those of kda_chunk_fwd_varlen without the
+ * workspace pair. Problems whose kda_chunk_fwd_varlen_workspace_size exceeds
+ * KDA_NOALLOC_SCRATCH_BYTES are refused with KDA_ERR_WORKSPACE before anything
+ * is launched (the 4 MiB array covers up to 524,256 tokens, B*T, for either
+ * dtype).
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (with it current) and caches it; make that first call before any
+ * stream capture. Every call shares the one array and leaves its contents
+ * behind; the kernels rewrite all scratch they read, so stale contents do not
+ * matter, but calls whose kernels overlap on the GPU race on the array: issue
+ * them on one stream, or order them.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+kda_status_t kda_chunk_fwd_varlen_noalloc(const void *q, const void *k, const void *v,
+                                          const void *g, const void *beta,
+                                          const int32_t *segment_ids, int64_t B, int64_t T,
+                                          int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                          kda_dtype_t dtype, kda_dtype_t out_dtype, void *o,
+                                          uint32_t *status_dev, kda_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char *kda_status_string(kda_status_t status);
 

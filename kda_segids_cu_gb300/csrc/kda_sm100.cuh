@@ -38,13 +38,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
         ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// One test of the phase with the given parity. If it has not completed, the thread
+// may be suspended (without issuing) for up to `suspend_ns` nanoseconds; it resumes
+// as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity,
+                                              uint32_t suspend_ns = 1000000u) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns) : "memory");
     return ok != 0;
 }
 
@@ -55,15 +59,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Bounded wait: returns false if the phase has not completed after `timeout_ns`
-// nanoseconds of wall time (each try_wait also suspends for a hardware-chosen
-// interval, so the clock is read only every 256 polls).
+// nanoseconds of wall time. Each poll may suspend the thread (see mbar_try_wait),
+// so waiting warps take no issue slots from working ones.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           uint64_t timeout_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
+        if ((i & 15u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
     }
 }
 

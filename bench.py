@@ -78,6 +78,29 @@ def chunk_flops_per_token_head(wl: synth.Workload) -> int:
     return 2 * C * (wl.d_qk + wl.d_v) + 4 * wl.d_qk * wl.d_v
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one chunk-kernel
+# launch on the ling3 workload, from an ncu capture of
+# `python bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline`. It holds only
+# for the kernel sources it was taken on (SHA-1 over the two files below);
+# after any change to them the bench reports null until a new capture.
+CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "7c70dfa686ec0ce5bbf5c991b42308ab544c8f9c",
+                 "read": 553_673_984, "write": 117_569_024}
+CHUNK_SOURCES = ("kda_segids_cu_gb300/csrc/kda_chunk_tc.cu", "kda_segids_cu_gb300/csrc/kda_sm100.cuh")
+
+
+def chunk_traffic(wl: synth.Workload):
+    import hashlib
+    if wl.name != CHUNK_TRAFFIC["workload"]:
+        return None
+    h = hashlib.sha1()
+    for p in CHUNK_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != CHUNK_TRAFFIC["sha1"]:
+        return None
+    return CHUNK_TRAFFIC["read"] + CHUNK_TRAFFIC["write"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -87,29 +110,108 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """SM clock and clock-event reasons sampled DURING the timed region.
 
+    NVML is read through ctypes every 2 ms from a thread (the library ships with
+    the driver); `mark_start`/`mark_stop` bracket the timed region on the host
+    after a device synchronize, and only samples inside the bracket count. If
+    NVML cannot be opened, `nvidia-smi -lms 200` is used instead (its samples
+    cover the whole sampling window)."""
+
+    # nvmlClocksEventReasons bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, cuda_index: int, period_s: float = 0.002):
+        self.cuda_index = cuda_index
+        self.period = period_s
+        self.samples = []          # (host time, sm MHz, reasons bitmask)
+        self.t_start = self.t_stop = None
+        self.thread = None
+        self.stop_flag = None
+        self.nvml = None
+        self.dev = None
+        self.max_mhz = None
         self.proc = None
         self.path = None
 
+    def _open_nvml(self) -> bool:
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if lib.nvmlInit_v2() != 0:
+            return False
+        dev = ctypes.c_void_p()
+        ok = False
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.cuda_index).uuid)
+            ok = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(dev)) == 0
+        except Exception:
+            ok = False
+        if not ok and "CUDA_VISIBLE_DEVICES" not in os.environ:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.cuda_index), ctypes.byref(dev)) == 0
+        if not ok:
+            return False
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx)) != 0:   # NVML_CLOCK_SM = 1
+            return False
+        self.nvml, self.dev, self.max_mhz = lib, dev, float(mx.value)
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return True
+
+    def _loop(self):
+        import ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            a = self.nvml.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk))
+            b = self.reasons_fn(self.dev, ctypes.byref(rs))
+            if a == 0 and b == 0:
+                self.samples.append((time.perf_counter(), float(clk.value), int(rs.value)))
+            time.sleep(self.period)
+
     def start(self):
+        import threading
+        if self._open_nvml():
+            self.stop_flag = threading.Event()
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+            return
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                ["nvidia-smi", f"--id={self.cuda_index}", f"--query-gpu={self.QUERY}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(1.0)        # let the first rows arrive
         except (OSError, FileNotFoundError):
             self.proc = None
 
+    def mark_start(self):
+        self.t_start = time.perf_counter()
+
+    def mark_stop(self):
+        self.t_stop = time.perf_counter()
+
     def stop(self) -> dict | None:
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=2)
+            inside = [s for s in self.samples if self.t_start <= s[0] <= self.t_stop]
+            if not inside:
+                return None
+            reasons = sorted({n for s in inside for bit, n in self.REASONS.items() if s[2] & bit})
+            return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(inside), "source": "nvml, 2 ms"}
+        return self._stop_smi()
+
+    def _stop_smi(self) -> dict | None:
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -129,15 +231,14 @@ class ClockSampler:
         os.unlink(self.path)
         if not rows:
             return None
-        sm = [r[0] for r in rows]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             for n, v in zip(names, r[2]):
                 if v.lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows)}
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "source": "nvidia-smi, 200 ms"}
 
 
 def make_step_inputs(wl: synth.Workload, device):
@@ -192,6 +293,7 @@ def run_gb300(args):
     clocks.start()
     barrier(ws)
     torch.cuda.synchronize()
+    clocks.mark_start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -199,6 +301,7 @@ def run_gb300(args):
         step(record=True)
     t1.record(stream)
     torch.cuda.synchronize()
+    clocks.mark_stop()
     barrier(ws)
     clk = clocks.stop()
     ms_local = t0.elapsed_time(t1) / args.steps
@@ -276,7 +379,7 @@ def run_gb300(args):
                    "l2": "inputs larger than L2 (chunk inputs 537 MB, conv inputs 403 MB)",
                    "parallelism": f"replicas x{ws} (rows independent)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None,
+                     "frac": achieved / hbm, "traffic": chunk_traffic(wl),
                      "kernel": "kda_chunk_fwd_varlen (planner + chunk kernel)",
                      "chunk_ms": chunk_ms, "bytes_per_launch": bytes_launch,
                      "flops_per_launch": flops_launch,
@@ -305,22 +408,28 @@ def cpu_baseline(wl: synth.Workload, seconds: float = 15.0, seed_heads: int | No
     h = seed_heads or wl.H
     f = 512
     kin = synth.make_kda_inputs(wl, heads=h)
-    t = time.perf_counter()
-    oracle.cu_seqlens(seg_np, wl.max_segs)
-    t_cu = time.perf_counter() - t
     ci = synth.make_conv_inputs(wl, features=f)
-    t = time.perf_counter()
-    oracle.short_conv(ci.x, ci.w, ci.segment_ids)
-    t_conv = time.perf_counter() - t
-    t = time.perf_counter()
-    oracle.kda_fwd(kin.q, kin.k, kin.v, kin.g, kin.beta, seg, wl.B, wl.T, n_threads=nt)
-    t_kda = time.perf_counter() - t
+    # repeat the sample until `seconds` of CPU work have been timed (at least once)
+    reps, t_cu, t_conv, t_kda = 0, 0.0, 0.0, 0.0
+    while reps == 0 or (t_cu + t_conv + t_kda < seconds and reps < 100):
+        t = time.perf_counter()
+        oracle.cu_seqlens(seg_np, wl.max_segs)
+        t_cu += time.perf_counter() - t
+        t = time.perf_counter()
+        oracle.short_conv(ci.x, ci.w, ci.segment_ids)
+        t_conv += time.perf_counter() - t
+        t = time.perf_counter()
+        oracle.kda_fwd(kin.q, kin.k, kin.v, kin.g, kin.beta, seg, wl.B, wl.T, n_threads=nt)
+        t_kda += time.perf_counter() - t
+        reps += 1
+    measured = t_cu + t_conv + t_kda
+    t_cu, t_conv, t_kda = t_cu / reps, t_conv / reps, t_kda / reps
     full = t_cu + 3 * t_conv * (wl.F / f) + t_kda * (wl.H / h)
     return {"value": wl.N / full, "unit": UNIT, "cores": nt, "kind": "oracle",
             "sample": f"{wl.name}: cu_seqlens in full; 1 conv on {f} of {wl.F} features "
                       f"(x3 convs, scaled by features); recurrence on {h} of {wl.H} heads "
                       f"(all {wl.N} tokens, {nt} threads, scaled by heads); "
-                      f"measured {t_cu + t_conv + t_kda:.1f} s",
+                      f"{reps} repetitions, measured {measured:.1f} s",
             "seconds_full_step_estimate": full}
 
 
@@ -372,13 +481,13 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default="ling3", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

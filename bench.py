@@ -385,7 +385,7 @@ def run_gb300(args):
                      "flops_per_launch": flops_launch,
                      "tensor_frac": flops_launch / (chunk_ms / 1e3) / (tf * 1e12),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
-        "gpu_launches": args.steps * 6,
+        "gpu_launches": args.steps * 7,
         "clocks": clk,
         "e2e": e2e,
     }

@@ -37,14 +37,44 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(x);
 }
 
+// Exact test "p is a multiple of T" for 0 <= p < 2^63 without a division:
+// write T = 2^s d with d odd; p is a multiple of T iff its low s bits are zero
+// and (p >> s) * d^-1 mod 2^64 <= (2^64 - 1) / d (divisibility by an odd
+// invariant integer through its inverse modulo 2^64: Granlund and Montgomery,
+// "Division by invariant integers using multiplication", PLDI 1994, sec. 9).
+struct RowStartTest {
+    uint64_t inv;    // d^-1 mod 2^64
+    uint64_t lim;    // (2^64 - 1) / d
+    uint64_t low;    // 2^s - 1
+    int shift;       // s
+
+    static RowStartTest make(int64_t T) {   // host side, T >= 1
+        RowStartTest r;
+        uint64_t t = uint64_t(T);
+        r.shift = 0;
+        while ((t & 1u) == 0) { t >>= 1; ++r.shift; }
+        uint64_t x = t;                       // Newton's iteration for the inverse
+        for (int i = 0; i < 6; ++i) x *= 2u - t * x;   // correct bits: 3, 6, 12, ... >= 64
+        r.inv = x;
+        r.lim = ~uint64_t(0) / t;
+        r.low = (uint64_t(1) << r.shift) - 1u;
+        return r;
+    }
+    __host__ __device__ __forceinline__ bool operator()(int64_t p) const {
+        const uint64_t u = uint64_t(p);
+        return (u & low) == 0 && (u >> shift) * inv <= lim;
+    }
+};
+
 // A token starts a segment when it is real (id != 0) and is the first token
 // of its row or its id differs from the previous token's ([RFC-0026] §3.1.1).
 // With no ids, each row is one segment: only row starts are starts.
-__device__ __forceinline__ bool is_segment_start(const int32_t* seg, int64_t p, int64_t T) {
-    if (seg == nullptr) return (p % T) == 0;
+__device__ __forceinline__ bool is_segment_start(const int32_t* seg, int64_t p,
+                                                 const RowStartTest& row_start) {
+    if (seg == nullptr) return row_start(p);
     const int32_t s = seg[p];
     if (s == 0) return false;
-    return (p % T) == 0 || seg[p - 1] != s;
+    return row_start(p) || seg[p - 1] != s;
 }
 
 __device__ __forceinline__ bool is_real(const int32_t* seg, int64_t p) {

@@ -31,7 +31,7 @@ constexpr int kListWarps = kListThreads / 32;
 // the segment count to counters[0]. A token p is the last of its segment when
 // it is real and p+1 is the end of the array, a row start, or carries another id.
 __global__ void __launch_bounds__(kListThreads, 1)
-list_segments_kernel(const int32_t* __restrict__ seg, int64_t N, int64_t T,
+list_segments_kernel(const int32_t* __restrict__ seg, int64_t N, RowStartTest row_start,
                      int32_t* __restrict__ seg_start, int32_t* __restrict__ seg_end,
                      int32_t* __restrict__ counters) {
     __shared__ int counts[kListItems][kListWarps];
@@ -50,9 +50,9 @@ list_segments_kernel(const int32_t* __restrict__ seg, int64_t N, int64_t T,
             st[i] = false;
             last[i] = false;
             if (p < N && is_real(seg, p)) {
-                st[i] = is_segment_start(seg, p, T);
+                st[i] = is_segment_start(seg, p, row_start);
                 const int64_t nx = p + 1;
-                last[i] = nx == N || (nx % T) == 0 || (seg != nullptr && seg[nx] != seg[p]);
+                last[i] = nx == N || row_start(nx) || (seg != nullptr && seg[nx] != seg[p]);
             }
         }
         unsigned m[kListItems];
@@ -193,7 +193,8 @@ static kda_status_t launch_recurrent_typed(const void* q, const void* k, const v
     int32_t* seg_start = static_cast<int32_t*>(ws);
     int32_t* seg_end = seg_start + N;
     int32_t* counters = seg_end + N;
-    list_segments_kernel<<<1, kListThreads, 0, stream>>>(seg, N, T_len, seg_start, seg_end,
+    list_segments_kernel<<<1, kListThreads, 0, stream>>>(seg, N, RowStartTest::make(T_len),
+                                                         seg_start, seg_end,
                                                          counters);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
     if (seg != nullptr) {

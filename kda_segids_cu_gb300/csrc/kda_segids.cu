@@ -8,108 +8,120 @@
 // t = 0 always starts a segment), and the last real segment ends one past the
 // last non-padding token.
 //
-// Design: one CTA of 1024 threads streams the ids in tiles of 16384 tokens
-// (16 independent loads in flight per thread). Start flags are ranked with
-// warp ballots + popc and a 512-entry scan of per-(item, warp) counts, so the
-// k-th start lands in cu_seqlens[k] by a direct scatter: no scratch memory and
-// no second pass. The tile order is item-major, so the ranks are the global
-// order of the flattened sequence.
+// Design: one CTA of 1024 threads walks the ids in tiles of 32768 tokens; each
+// thread owns a contiguous run of 32 ids, read with eight 16-byte loads (one
+// round trip per tile), and takes the previous token's id from its own run or,
+// for its first token, from the neighbouring thread (a shuffle, or shared memory
+// across warps and tiles). Each thread ranks its starts with a block-wide
+// exclusive scan of per-thread counts, so the k-th start lands in cu_seqlens[k]
+// by a direct scatter in token order: no scratch memory and no second pass.
 #include "kda_common.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kItems = 16;
+constexpr int kRun = 32;                           // ids per thread per tile
 constexpr int kWarps = kThreads / 32;
-constexpr int64_t kTile = int64_t(kThreads) * kItems;
+constexpr int64_t kTile = int64_t(kThreads) * kRun;
 
 __global__ void __launch_bounds__(kThreads, 1)
-segids_to_cu_seqlens_kernel(const int32_t* __restrict__ seg, int64_t N, int64_t T,
+segids_to_cu_seqlens_kernel(const int32_t* __restrict__ seg, int64_t N, RowStartTest row_start,
                             int32_t max_segs, int32_t* __restrict__ cu,
                             int32_t* __restrict__ n_segs_out) {
-    __shared__ int counts[kItems][kWarps];
-    __shared__ int offsets[kItems][kWarps];
+    __shared__ int warp_sum[kWarps];
+    __shared__ int32_t warp_last_id[kWarps];       // last id of each warp's last thread
     __shared__ int tile_total;
-    __shared__ int warp_last[kWarps];
+    __shared__ int32_t carry_id;                   // last id of the previous tile
+    __shared__ int red[kWarps];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const unsigned lt_mask = (1u << lane) - 1u;
 
     int64_t running = 0;      // starts in earlier tiles (same value in every thread)
-    int last_real_end = 0;    // max over real tokens of p + 1 (thread-local)
+    int64_t last_real_end = 0;
+    const bool vec = (reinterpret_cast<uintptr_t>(seg) & 15u) == 0;   // 16-byte loads allowed
+    if (threadIdx.x == 0) carry_id = 0;
 
     for (int64_t base = 0; base < N; base += kTile) {
-        bool st[kItems];
+        const int64_t p0 = base + int64_t(threadIdx.x) * kRun;
+        int32_t id[kRun];
+        if (vec && p0 + kRun <= N) {
+            const int4* src = reinterpret_cast<const int4*>(seg + p0);
 #pragma unroll
-        for (int i = 0; i < kItems; ++i) {
-            const int64_t p = base + int64_t(i) * kThreads + threadIdx.x;
-            bool s = false;
-            if (p < N) {
-                const int32_t id = seg[p];
-                if (id != 0) {
-                    last_real_end = max(last_real_end, int(p + 1));
-                    s = (p % T) == 0 || seg[p - 1] != id;
-                }
+            for (int i = 0; i < kRun / 4; ++i) {
+                const int4 v = src[i];
+                id[4 * i] = v.x; id[4 * i + 1] = v.y; id[4 * i + 2] = v.z; id[4 * i + 3] = v.w;
             }
-            st[i] = s;
-        }
-        unsigned m[kItems];
+        } else {
 #pragma unroll
-        for (int i = 0; i < kItems; ++i) {
-            m[i] = __ballot_sync(0xffffffffu, st[i]);
-            if (lane == 0) counts[i][warp] = __popc(m[i]);
+            for (int i = 0; i < kRun; ++i) id[i] = (p0 + i < N) ? seg[p0 + i] : 0;
         }
+        // id of the token before this run
+        int32_t prev = __shfl_up_sync(0xffffffffu, id[kRun - 1], 1);
+        if (lane == 31) warp_last_id[warp] = id[kRun - 1];
+        __syncthreads();                            // also orders carry_id from the last tile
+        if (lane == 0) prev = (warp == 0) ? carry_id : warp_last_id[warp - 1];
+        unsigned mask = 0;
+#pragma unroll
+        for (int i = 0; i < kRun; ++i) {
+            const int64_t p = p0 + i;
+            const int32_t before = (i == 0) ? prev : id[i - 1];
+            const bool real = p < N && id[i] != 0;
+            if (real) last_real_end = p + 1;
+            const bool st = real && (row_start(p) || before != id[i]);
+            mask |= unsigned(st) << i;
+        }
+        // block exclusive scan of the per-thread start counts
+        const int cnt = __popc(mask);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (lane == 31) warp_sum[warp] = incl;
         __syncthreads();
         if (warp == 0) {
-            // lane l scans flattened entries [16 l, 16 l + 16) of counts (item-major)
-            int vals[16];
-            int sum = 0;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int idx = lane * 16 + j;
-                vals[j] = counts[idx / kWarps][idx % kWarps];
-                sum += vals[j];
-            }
-            int incl = sum;
+            const int ws = warp_sum[lane];
+            int wi = ws;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += n;
+                const int n = __shfl_up_sync(0xffffffffu, wi, o);
+                if (lane >= o) wi += n;
             }
-            int excl = incl - sum;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int idx = lane * 16 + j;
-                offsets[idx / kWarps][idx % kWarps] = excl;
-                excl += vals[j];
-            }
-            if (lane == 31) tile_total = incl;
+            warp_sum[lane] = wi - ws;
+            if (lane == 31) tile_total = wi;
         }
         __syncthreads();
-#pragma unroll
-        for (int i = 0; i < kItems; ++i) {
-            if (st[i]) {
-                const int64_t p = base + int64_t(i) * kThreads + threadIdx.x;
-                const int64_t rank = running + offsets[i][warp] + __popc(m[i] & lt_mask);
-                // cu[r] = start of the (r+1)-th segment, for 1 <= r < max_segs
-                if (rank >= 1 && rank < max_segs) cu[rank] = int32_t(p);
-            }
+        int64_t rank = running + warp_sum[warp] + (incl - cnt);
+        while (mask) {
+            const int i = __ffs(mask) - 1;
+            mask &= mask - 1;
+            // cu[r] = start of the (r+1)-th segment, for 1 <= r < max_segs
+            if (rank >= 1 && rank < max_segs) cu[rank] = int32_t(p0 + i);
+            ++rank;
         }
         running += tile_total;
-        __syncthreads();   // counts/offsets are rewritten by the next tile
+        if (threadIdx.x == kThreads - 1) carry_id = id[kRun - 1];
+        __syncthreads();   // warp_sum / tile_total / carry_id are rewritten by the next tile
     }
 
     // block max of the end of the last real token
-    int v = __reduce_max_sync(0xffffffffu, last_real_end);
-    if (lane == 0) warp_last[warp] = v;
+    int64_t v = last_real_end;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const int64_t n = __shfl_xor_sync(0xffffffffu, v, o);
+        v = n > v ? n : v;
+    }
+    if (lane == 0) red[warp] = int(v);
     __syncthreads();
     if (warp == 0) {
-        v = __reduce_max_sync(0xffffffffu, warp_last[lane]);
-        if (lane == 0) warp_last[0] = v;
+        int m = red[lane];
+        m = __reduce_max_sync(0xffffffffu, m);
+        if (lane == 0) red[0] = m;
     }
     __syncthreads();
-    const int64_t n_end = warp_last[0];
+    const int64_t n_end = red[0];
     const int64_t n = running;
     for (int64_t i = threadIdx.x; i <= max_segs; i += kThreads) {
         if (i == 0) {
@@ -129,7 +141,7 @@ segids_to_cu_seqlens_kernel(const int32_t* __restrict__ seg, int64_t N, int64_t 
 kda_status_t kda_launch_segids_to_cu_seqlens(const int32_t* seg, int64_t B, int64_t T,
                                              int32_t max_segs, int32_t* cu, int32_t* n_segs,
                                              cudaStream_t stream) {
-    kda::segids_to_cu_seqlens_kernel<<<1, kda::kThreads, 0, stream>>>(seg, B * T, T, max_segs,
-                                                                      cu, n_segs);
+    kda::segids_to_cu_seqlens_kernel<<<1, kda::kThreads, 0, stream>>>(
+        seg, B * T, kda::RowStartTest::make(T), max_segs, cu, n_segs);
     return kda::launch_status();
 }

@@ -4,25 +4,75 @@
 // "ShortConvolution segment 边界 mask": y[b,t,f] = sum_j w[j,f] x[b,t-j,f] over
 // taps j < K whose source token t-j exists and carries the destination's id.
 //
-// Design (HBM-bound: 2 x sizeof(dtype) bytes per element): a CTA of 256 threads
+// Design (HBM-bound: 2 x sizeof(dtype) bytes per element): a CTA of 128 threads
 // owns a tile of kTok consecutive tokens of one row and 2 KB of features (1024
 // bf16 or 512 fp32). It stages the tile and its K-1 halo tokens in shared memory
-// with 16-byte asynchronous copies (cp.async: about 70 KB requested at once per
-// CTA, no registers held), then each thread takes one 16-byte feature vector
-// and half of the tile's tokens, slides a window of K-1 unpacked inputs along
-// them and stores 16-byte outputs, coalesced along F. Halo tokens are re-read,
-// mostly from L2. Products accumulate in fp32 and round once to the output.
+// with 16-byte asynchronous copies (cp.async: the whole tile requested at once, no
+// registers held), then each thread takes one 16-byte feature vector, slides a
+// window of K-1 unpacked inputs along the tile's tokens (fully unrolled, packed
+// fp32x2 arithmetic) and stores 16-byte outputs,
+// coalesced along F. Small tiles let several CTAs per SM keep loads in flight while
+// others compute. Halo tokens are re-read, mostly from L2. Products accumulate in
+// fp32 and round once to the output.
 #include "kda_common.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kTok = 32;               // tokens per tile
+constexpr int kTok = 16;               // tokens per tile
 constexpr int kTileBytes = 2048;       // feature bytes per tile row
 constexpr int kCols = kTileBytes / 16; // 16-byte feature vectors per tile row
-constexpr int kConvThreads = 2 * kCols;
+constexpr int kConvThreads = kCols;       // one thread per 16-byte feature vector
 
 template <typename T> struct Vec;
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 u, v, w;\n\tmov.b64 u, {%2, %3};\n\tmov.b64 v, {%4, %5};\n\t"
+        "mul.rn.f32x2 w, u, v;\n\tmov.b64 {%0, %1}, w;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 u, v, w, z;\n\tmov.b64 u, {%2, %3};\n\tmov.b64 v, {%4, %5};\n\t"
+        "mov.b64 w, {%6, %7};\n\tfma.rn.f32x2 z, u, v, w;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// 16-byte vectors as pairs of fp32 values (P pairs).
+template <typename T> struct Pairs;
+template <> struct Pairs<__nv_bfloat16> {
+    static constexpr int P = 4;
+    __device__ static void cvt(const uint4& u, float2 (&o)[P]) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)     // bf16 -> fp32 is exact: the bits are the top half
+            o[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+    }
+    __device__ static uint4 pack(const float2 (&a)[P]) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a[i].x, a[i].y);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+template <> struct Pairs<float> {
+    static constexpr int P = 2;
+    __device__ static void cvt(const uint4& u, float2 (&o)[P]) {
+        o[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+        o[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+    }
+    __device__ static uint4 pack(const float2 (&a)[P]) {
+        return make_uint4(__float_as_uint(a[0].x), __float_as_uint(a[0].y), __float_as_uint(a[1].x),
+                          __float_as_uint(a[1].y));
+    }
+};
+
 template <> struct Vec<__nv_bfloat16> {
     static constexpr int N = 8;
     __device__ static void load(const void* p, float* out) {
@@ -68,7 +118,7 @@ template <int K>
 constexpr int conv_smem_bytes() { return (kTok + K - 1) * kTileBytes; }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads, (K <= 5 ? 3 : 2))
+__global__ void __launch_bounds__(kConvThreads, (K <= 5 ? 5 : 2))
 short_conv_kernel(const T* __restrict__ x, const T* __restrict__ w,
                   const int32_t* __restrict__ seg, T* __restrict__ y, int64_t T_len,
                   int64_t F, int64_t tiles_per_row) {
@@ -97,53 +147,54 @@ short_conv_kernel(const T* __restrict__ x, const T* __restrict__ w,
         const int64_t t = t0 - Hl + u;
         ids[u] = (seg && t >= 0 && t < T_len) ? seg[row + t] : 0;
     }
-    const int c = threadIdx.x % kCols;          // this thread's feature vector
-    const int half = threadIdx.x / kCols;       // tokens [16 half, 16 half + 16) of the tile
-    float wr[K][V];
+    const int c = threadIdx.x;                  // this thread's feature vector
+    constexpr int P = Pairs<T>::P;
+    float2 wp[K][P];                            // the K taps of this vector, as pairs
     if (c < cols) {
 #pragma unroll
-        for (int j = 0; j < K; ++j) Vec<T>::load(w + int64_t(j) * F + fb + c * V, wr[j]);
+        for (int j = 0; j < K; ++j)
+            Pairs<T>::cvt(*reinterpret_cast<const uint4*>(w + int64_t(j) * F + fb + c * V), wp[j]);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     if (c >= cols) return;
 
-    constexpr int kHalf = kTok / 2;
-    const int r0 = half * kHalf;                // first output of this thread, tile-relative
-    // window[j] holds the raw 16 bytes of token r - 1 - j (tile-relative r); they are
-    // unpacked where used, which keeps the window at 4 registers per token
-    uint4 win[K > 1 ? K - 1 : 1];
+    // The tile's tokens, fully unrolled: win[j] holds the unpacked input of token r-1-j,
+    // so each input is converted once and the window shifts by renaming registers.
+    // Rows past the end of the row were not staged: they are never stored and never
+    // feed a stored output (sources precede their destinations).
+    float2 win[K > 1 ? K - 1 : 1][P];
 #pragma unroll
     for (int j = 0; j < Hl; ++j)
-        win[j] = *reinterpret_cast<const uint4*>(tile + (Hl + r0 - 1 - j) * kTileBytes + c * 16);
-#pragma unroll 1
-    for (int r = r0; r < r0 + kHalf; ++r) {
+        Pairs<T>::cvt(*reinterpret_cast<const uint4*>(tile + (Hl - 1 - j) * kTileBytes + c * 16), win[j]);
+#pragma unroll
+    for (int r = 0; r < kTok; ++r) {
         const int u = Hl + r;
         const int64_t t = t0 + r;
-        if (t >= T_len) break;
-        const uint4 cur_raw = *reinterpret_cast<const uint4*>(tile + u * kTileBytes + c * 16);
+        float2 cur[P];
+        Pairs<T>::cvt(*reinterpret_cast<const uint4*>(tile + u * kTileBytes + c * 16), cur);
         const int32_t id = ids[u];
-        float acc[V];
-        {
-            float cur[V];
-            Vec<T>::cvt(cur_raw, cur);
+        float2 acc[P];
 #pragma unroll
-            for (int e = 0; e < V; ++e) acc[e] = wr[0][e] * cur[e];
-        }
+        for (int p = 0; p < P; ++p) acc[p] = mul2(wp[0][p], cur[p]);
 #pragma unroll
         for (int j = 0; j < Hl; ++j) {
             // source token t - 1 - j exists (t - 1 - j >= 0) and carries the same id
             if (t - 1 - j >= 0 && ids[u - 1 - j] == id) {
-                float src[V];
-                Vec<T>::cvt(win[j], src);
 #pragma unroll
-                for (int e = 0; e < V; ++e) acc[e] = fmaf(wr[j + 1][e], src[e], acc[e]);
+                for (int p = 0; p < P; ++p) acc[p] = fma2(wp[j + 1][p], win[j][p], acc[p]);
             }
         }
-        Vec<T>::store(y + (row + t) * F + fb + c * V, acc);
+        if (t < T_len) *reinterpret_cast<uint4*>(y + (row + t) * F + fb + c * V) = Pairs<T>::pack(acc);
 #pragma unroll
-        for (int j = Hl - 1; j > 0; --j) win[j] = win[j - 1];
-        if (Hl > 0) win[0] = cur_raw;
+        for (int j = Hl - 1; j > 0; --j) {
+#pragma unroll
+            for (int p = 0; p < P; ++p) win[j][p] = win[j - 1][p];
+        }
+        if (Hl > 0) {
+#pragma unroll
+            for (int p = 0; p < P; ++p) win[0][p] = cur[p];
+        }
     }
 }
 

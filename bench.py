@@ -322,35 +322,67 @@ def run_gb300(args):
         host_out = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory()}
         for i in range(3):
             host_out[f"y{i}"] = torch.empty(ys[i].shape, dtype=ys[i].dtype).pin_memory()
-        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
         h2d = sum(v.numel() * v.element_size() for v in host_in.values())
         d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+        # Steps are pipelined: two copy streams bring step i's inputs in while the
+        # compute stream runs step i-1 and a third stream copies step i-1's outputs
+        # out; device inputs and outputs are double-buffered, ordered by events.
+        nb = 2
+        dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(nb)]
+        dev_out = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in host_out.items()}
+                   for _ in range(nb)]
+        s_in = [torch.cuda.Stream(device=dev) for _ in range(2)]
+        s_out = torch.cuda.Stream(device=dev)
+        keys = sorted(host_in, key=lambda k: -host_in[k].numel() * host_in[k].element_size())
+        ev_comp = [None] * nb       # kernels of the step that last used buffer b are done
+        ev_out = [None] * nb        # outputs of the step that last used buffer b are copied out
 
-        def e2e_step():
-            for k, v in host_in.items():
-                dev_in[k].copy_(v, non_blocking=True)
-            kda.kda_segids_to_cu_seqlens(dev_in["seg"], wl.max_segs, out=cu, n_segs_out=nseg)
-            for i in range(3):
-                kda.kda_short_conv_varlen(dev_in[f"x{i}"], dev_in[f"w{i}"], dev_in["seg"], out=ys[i])
-            kda.kda_chunk_fwd_varlen(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"],
-                                     dev_in["beta"], dev_in["seg"], B=wl.B, T=wl.T, out=o,
-                                     workspace=work, status=status)
-            host_out["o"].copy_(o, non_blocking=True)
-            for i in range(3):
-                host_out[f"y{i}"].copy_(ys[i], non_blocking=True)
+        def e2e_step(i):
+            b = i % nb
+            for si in s_in:
+                if ev_comp[b] is not None:
+                    si.wait_event(ev_comp[b])
+            for j, k in enumerate(keys):
+                with torch.cuda.stream(s_in[j % len(s_in)]):
+                    dev_in[b][k].copy_(host_in[k], non_blocking=True)
+            for si in s_in:
+                e = torch.cuda.Event()
+                e.record(si)
+                stream.wait_event(e)
+            if ev_out[b] is not None:
+                stream.wait_event(ev_out[b])
+            d_in, d_out = dev_in[b], dev_out[b]
+            kda.kda_segids_to_cu_seqlens(d_in["seg"], wl.max_segs, out=cu, n_segs_out=nseg)
+            for c in range(3):
+                kda.kda_short_conv_varlen(d_in[f"x{c}"], d_in[f"w{c}"], d_in["seg"], out=d_out[f"y{c}"])
+            kda.kda_chunk_fwd_varlen(d_in["q"], d_in["k"], d_in["v"], d_in["g"], d_in["beta"],
+                                     d_in["seg"], B=wl.B, T=wl.T, out=d_out["o"], workspace=work,
+                                     status=status)
+            ev_comp[b] = torch.cuda.Event()
+            ev_comp[b].record(stream)
+            s_out.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_out):
+                for k, v in host_out.items():
+                    v.copy_(d_out[k], non_blocking=True)
+            ev_out[b] = torch.cuda.Event()
+            ev_out[b].record(s_out)
 
-        for _ in range(min(args.warmup, 3)):
-            e2e_step()
+        for i in range(min(args.warmup, 3)):
+            e2e_step(i)
         torch.cuda.synchronize()
+        ev_comp, ev_out = [None] * nb, [None] * nb
         barrier(ws)
         a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
+        b_ev = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        b.record(stream)
+        for si in s_in + [s_out]:
+            si.wait_event(a)
+        for i in range(args.steps):
+            e2e_step(i)
+        stream.wait_event(ev_out[(args.steps - 1) % nb])
+        b_ev.record(stream)
         torch.cuda.synchronize()
-        e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, ws, dev)
+        e_ms = max_over_ranks(a.elapsed_time(b_ev) / args.steps, ws, dev)
         e2e = {"value": N * ws / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 

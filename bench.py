@@ -64,6 +64,14 @@ def max_over_ranks(x: float, ws: int, device) -> float:
     return float(t.item())
 
 
+def job_throughput(units_per_rank: int, ms_local: float, ws: int, device):
+    """Whole-job throughput of a weak-scaling run: every rank processes
+    `units_per_rank` units; the job takes as long as its slowest rank.
+    Returns (units per second over all ranks, slowest rank's ms)."""
+    ms = max_over_ranks(ms_local, ws, device)
+    return units_per_rank * ws / (ms / 1e3), ms
+
+
 def chunk_bytes_per_token_head(wl: synth.Workload) -> int:
     """Algorithmic HBM bytes of kda_chunk_fwd_varlen per (token, head): q, k, g
     (d_qk each), v and o (d_v each) and beta, in the workload dtype."""
@@ -270,20 +278,28 @@ def run_gb300(args):
     wsb = kda.chunk_fwd_workspace_bytes(wl.B, wl.T, H, wl.d_qk, wl.d_v, wl.dtype)
     work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ev_chunk = []
+    ev_chunk, ev_seg, ev_conv = [], [], []
+
+    def mark(record):
+        if not record:
+            return None
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        return e
 
     def step(record=False):
+        a = mark(record)
         kda.kda_segids_to_cu_seqlens(seg, wl.max_segs, out=cu, n_segs_out=nseg)
+        b = mark(record)
         for c, y in zip(convs, ys):
             kda.kda_short_conv_varlen(c.x, c.w, c.segment_ids, out=y)
-        if record:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
+        e0 = mark(record)
         kda.kda_chunk_fwd_varlen(kin.q, kin.k, kin.v, kin.g, kin.beta, seg, B=wl.B, T=wl.T,
                                  out=o, workspace=work, status=status)
+        e1 = mark(record)
         if record:
-            e1.record(stream)
+            ev_seg.append((a, b))
+            ev_conv.append((b, e0))
             ev_chunk.append((e0, e1))
 
     for _ in range(args.warmup):
@@ -305,8 +321,11 @@ def run_gb300(args):
     barrier(ws)
     clk = clocks.stop()
     ms_local = t0.elapsed_time(t1) / args.steps
-    ms = max_over_ranks(ms_local, ws, dev)
+    value, ms = job_throughput(N, ms_local, ws, dev)
     chunk_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_chunk)
+    seg_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_seg)
+    conv_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_conv) / len(convs)
+    real_tokens = int((seg != 0).sum().item())
     if int(status.item()) != 0:
         print(f"warning: device status {int(status.item()):#x}", file=sys.stderr)
 
@@ -382,8 +401,8 @@ def run_gb300(args):
         stream.wait_event(ev_out[(args.steps - 1) % nb])
         b_ev.record(stream)
         torch.cuda.synchronize()
-        e_ms = max_over_ranks(a.elapsed_time(b_ev) / args.steps, ws, dev)
-        e2e = {"value": N * ws / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e_value, e_ms = job_throughput(N, a.elapsed_time(b_ev) / args.steps, ws, dev)
+        e2e = {"value": e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
     if rank != 0:
@@ -394,7 +413,7 @@ def run_gb300(args):
     achieved = bytes_launch / (chunk_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
-        "value": N * ws / (ms / 1e3),
+        "value": value,
         "unit": UNIT,
         "n_gpus": ws,
         "steps": args.steps,
@@ -405,7 +424,7 @@ def run_gb300(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; Ling3-tiny packed shape, lognormal EOD-separated documents)",
-        "config": {"workload": f"ling3 packed: B={wl.B} T={wl.T} H={H} D={wl.d_qk} bf16, "
+        "config": {"workload": f"{wl.name} packed: B={wl.B} T={wl.T} H={H} D={wl.d_qk} bf16, "
                                f"max_segs={wl.max_segs}, conv width {wl.k_conv}",
                    "step": "segids->cu_seqlens + 3 masked short convs + chunked KDA fwd",
                    "l2": "inputs larger than L2 (chunk inputs 537 MB, conv inputs 403 MB)",
@@ -417,6 +436,15 @@ def run_gb300(args):
                      "flops_per_launch": flops_launch,
                      "tensor_frac": flops_launch / (chunk_ms / 1e3) / (tf * 1e12),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
+        "ops": {
+            name: {"us_per_call": ms_ * 1e3, "algorithmic_bytes": nbytes,
+                   "gbs": nbytes / (ms_ / 1e3) / 1e9, "frac_hbm": nbytes / (ms_ / 1e3) / 1e9 / hbm}
+            for name, ms_, nbytes in (
+                ("kda_segids_to_cu_seqlens", seg_ms, 4 * N),
+                ("kda_short_conv_varlen", conv_ms, 2 * N * wl.F * convs[0].x.element_size()),
+                ("kda_chunk_fwd_varlen", chunk_ms, bytes_launch))
+        },
+        "real_tokens_per_s": real_tokens * ws / (ms / 1e3),
         "gpu_launches": args.steps * 7,
         "clocks": clk,
         "e2e": e2e,
@@ -502,7 +530,7 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "impl": "reference",
-            "config": {"workload": f"ling3 packed: B={wl.B} T={wl.T} H={wl.H} D={wl.d_qk}",
+            "config": {"workload": f"{wl.name} packed: B={wl.B} T={wl.T} H={wl.H} D={wl.d_qk}",
                        "step": "fp64 CPU oracle: cu_seqlens + 3 masked convs + recurrence"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt, "kind": "oracle",
                              "sample": sample},

@@ -5,21 +5,23 @@
 // taps j < K whose source token t-j exists and carries the destination's id.
 //
 // Design (HBM-bound: 2 x sizeof(dtype) bytes per element): a CTA of 128 threads
-// owns a tile of kTok consecutive tokens of one row and 2 KB of features (1024
-// bf16 or 512 fp32). It stages the tile and its K-1 halo tokens in shared memory
-// with 16-byte asynchronous copies (cp.async: the whole tile requested at once, no
-// registers held), then each thread takes one 16-byte feature vector, slides a
-// window of K-1 unpacked inputs along the tile's tokens (fully unrolled, packed
-// fp32x2 arithmetic) and stores 16-byte outputs,
-// coalesced along F. Small tiles let several CTAs per SM keep loads in flight while
-// others compute. Halo tokens are re-read, mostly from L2. Products accumulate in
-// fp32 and round once to the output.
+// owns 2 KB of features (1024 bf16 or 512 fp32) of one row and streams a span of
+// its tokens, two CTAs per SM. Each thread owns one 16-byte feature vector and walks
+// the span in tiles of kTok tokens through a ring of kRing tiles in shared memory,
+// filled by 16-byte asynchronous copies (cp.async, kRing - 1 tiles requested ahead,
+// no registers held). A thread reads back only what it copied, so the ring needs no
+// barrier. It slides a window of K-1 unpacked inputs along the tokens (fully unrolled
+// per tile, packed fp32x2 arithmetic); the window carries across tiles, so only a
+// span's first K-1 tokens are read twice. Outputs are 16-byte stores, coalesced
+// along F. Products accumulate in fp32 and round once to the output.
 #include "kda_common.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kTok = 16;               // tokens per tile
+constexpr int kRing = 3;               // tiles of the ring (kRing - 1 in flight while one is used)
+constexpr int kConvCtasPerSm = 2;
 constexpr int kTileBytes = 2048;       // feature bytes per tile row
 constexpr int kCols = kTileBytes / 16; // 16-byte feature vectors per tile row
 constexpr int kConvThreads = kCols;       // one thread per 16-byte feature vector
@@ -114,96 +116,128 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
                      __cvta_generic_to_shared(smem))), "l"(gmem) : "memory");
 }
 
-template <int K>
-constexpr int conv_smem_bytes() { return (kTok + K - 1) * kTileBytes; }
+constexpr int conv_smem_bytes() { return kRing * kTok * kTileBytes; }
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads, (K <= 5 ? 5 : 2))
+__global__ void __launch_bounds__(kConvThreads, kConvCtasPerSm)
 short_conv_kernel(const T* __restrict__ x, const T* __restrict__ w,
                   const int32_t* __restrict__ seg, T* __restrict__ y, int64_t T_len,
-                  int64_t F, int64_t tiles_per_row) {
+                  int64_t F, int64_t span, int64_t spans_per_row) {
     constexpr int V = Vec<T>::N;
-    constexpr int Hl = K - 1;                  // halo tokens before the tile
-    constexpr int R = kTok + Hl;               // staged rows; row u holds token t0 - Hl + u
-    extern __shared__ __align__(16) uint8_t tile[];
-    __shared__ int32_t ids[R];
-    const int64_t b = blockIdx.x / tiles_per_row;      // token tiles along x, feature tiles along y
-    const int64_t t0 = (blockIdx.x % tiles_per_row) * kTok;
+    constexpr int Hl = K - 1;                  // window: the K-1 tokens before the current one
+    constexpr int P = Pairs<T>::P;
+    extern __shared__ __align__(16) uint8_t ring[];
+    const int64_t b = blockIdx.x / spans_per_row;      // (row, span) along x, feature block along y
+    const int64_t s0 = (blockIdx.x % spans_per_row) * span;
+    const int64_t s1 = (s0 + span < T_len) ? s0 + span : T_len;
     const int64_t fb = int64_t(blockIdx.y) * (kTileBytes / sizeof(T));   // first feature
-    const int64_t row = b * T_len;
     const int64_t f_left = F - fb;
     const int cols = f_left * int64_t(sizeof(T)) >= kTileBytes
                          ? kCols : int(f_left * int64_t(sizeof(T)) / 16);
-
-    // stage rows of tokens that exist (rows outside the row are never read below)
-    for (int i = threadIdx.x; i < R * kCols; i += kConvThreads) {
-        const int u = i / kCols, c = i % kCols;
-        const int64_t t = t0 - Hl + u;
-        if (c < cols && t >= 0 && t < T_len)
-            cp_async16(tile + u * kTileBytes + c * 16, x + (row + t) * F + fb + c * V);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    for (int u = threadIdx.x; u < R; u += kConvThreads) {
-        const int64_t t = t0 - Hl + u;
-        ids[u] = (seg && t >= 0 && t < T_len) ? seg[row + t] : 0;
-    }
     const int c = threadIdx.x;                  // this thread's feature vector
-    constexpr int P = Pairs<T>::P;
-    float2 wp[K][P];                            // the K taps of this vector, as pairs
-    if (c < cols) {
-#pragma unroll
-        for (int j = 0; j < K; ++j)
-            Pairs<T>::cvt(*reinterpret_cast<const uint4*>(w + int64_t(j) * F + fb + c * V), wp[j]);
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncthreads();
-    if (c >= cols) return;
+    if (c >= cols || s0 >= s1) return;          // no barrier below: leaving early is safe
+    const T* xc = x + b * T_len * F + fb + c * V;   // token t of this vector at xc + t * F
+    T* yc = y + b * T_len * F + fb + c * V;
+    const int32_t* sr = seg ? seg + b * T_len : nullptr;
+    uint8_t* mine = ring + c * 16;                  // this thread's column of every ring row
+    const int n_tiles = int((s1 - s0 + kTok - 1) / kTok);
 
-    // The tile's tokens, fully unrolled: win[j] holds the unpacked input of token r-1-j,
-    // so each input is converted once and the window shifts by renaming registers.
-    // Rows past the end of the row were not staged: they are never stored and never
-    // feed a stored output (sources precede their destinations).
+    auto issue = [&](int ti) {                  // tile ti of the span into ring slot ti % kRing
+        if (ti < n_tiles) {
+            const int64_t t0 = s0 + int64_t(ti) * kTok;
+            uint8_t* slot = mine + (ti % kRing) * (kTok * kTileBytes);
+#pragma unroll
+            for (int r = 0; r < kTok; ++r)
+                if (t0 + r < s1) cp_async16(slot + r * kTileBytes, xc + (t0 + r) * F);
+        }
+        cp_async_commit();                      // one group per tile, empty past the end
+    };
+#pragma unroll
+    for (int ti = 0; ti < kRing - 1; ++ti) issue(ti);
+
+    float2 wp[K][P];                            // the K taps of this vector, as pairs
+#pragma unroll
+    for (int j = 0; j < K; ++j)
+        Pairs<T>::cvt(*reinterpret_cast<const uint4*>(w + int64_t(j) * F + fb + c * V), wp[j]);
+    // the window before the span: win[j] is token s0-1-j, wid[j] its id
     float2 win[K > 1 ? K - 1 : 1][P];
+    int32_t wid[K > 1 ? K - 1 : 1];
 #pragma unroll
-    for (int j = 0; j < Hl; ++j)
-        Pairs<T>::cvt(*reinterpret_cast<const uint4*>(tile + (Hl - 1 - j) * kTileBytes + c * 16), win[j]);
+    for (int j = 0; j < Hl; ++j) {
+        const int64_t t = s0 - 1 - j;
+        if (t >= 0) {
+            Pairs<T>::cvt(*reinterpret_cast<const uint4*>(xc + t * F), win[j]);
+            wid[j] = sr ? sr[t] : 0;
+        } else {
 #pragma unroll
-    for (int r = 0; r < kTok; ++r) {
-        const int u = Hl + r;
-        const int64_t t = t0 + r;
-        float2 cur[P];
-        Pairs<T>::cvt(*reinterpret_cast<const uint4*>(tile + u * kTileBytes + c * 16), cur);
-        const int32_t id = ids[u];
-        float2 acc[P];
+            for (int p = 0; p < P; ++p) win[j][p] = make_float2(0.f, 0.f);
+            wid[j] = 0;
+        }
+    }
+
+    for (int ti = 0; ti < n_tiles; ++ti) {
+        issue(ti + kRing - 1);
+        const int64_t t0 = s0 + int64_t(ti) * kTok;
+        int32_t ids[kTok];
 #pragma unroll
-        for (int p = 0; p < P; ++p) acc[p] = mul2(wp[0][p], cur[p]);
+        for (int r = 0; r < kTok; ++r) ids[r] = (sr && t0 + r < s1) ? sr[t0 + r] : 0;
+        cp_async_wait<kRing - 1>();             // this tile's copies have landed
+        const uint8_t* slot = mine + (ti % kRing) * (kTok * kTileBytes);
 #pragma unroll
-        for (int j = 0; j < Hl; ++j) {
-            // source token t - 1 - j exists (t - 1 - j >= 0) and carries the same id
-            if (t - 1 - j >= 0 && ids[u - 1 - j] == id) {
+        for (int r = 0; r < kTok; ++r) {
+            const int64_t t = t0 + r;
+            if (t >= s1) break;
+            float2 cur[P];
+            Pairs<T>::cvt(*reinterpret_cast<const uint4*>(slot + r * kTileBytes), cur);
+            const int32_t id = ids[r];
+            float2 acc[P];
 #pragma unroll
-                for (int p = 0; p < P; ++p) acc[p] = fma2(wp[j + 1][p], win[j][p], acc[p]);
+            for (int p = 0; p < P; ++p) acc[p] = mul2(wp[0][p], cur[p]);
+#pragma unroll
+            for (int j = 0; j < Hl; ++j) {
+                // source token t - 1 - j exists (t - 1 - j >= 0) and carries the same id
+                if (t - 1 - j >= 0 && wid[j] == id) {
+#pragma unroll
+                    for (int p = 0; p < P; ++p) acc[p] = fma2(wp[j + 1][p], win[j][p], acc[p]);
+                }
+            }
+            *reinterpret_cast<uint4*>(yc + t * F) = Pairs<T>::pack(acc);
+#pragma unroll
+            for (int j = Hl - 1; j > 0; --j) {
+                wid[j] = wid[j - 1];
+#pragma unroll
+                for (int p = 0; p < P; ++p) win[j][p] = win[j - 1][p];
+            }
+            if (Hl > 0) {
+                wid[0] = id;
+#pragma unroll
+                for (int p = 0; p < P; ++p) win[0][p] = cur[p];
             }
         }
-        if (t < T_len) *reinterpret_cast<uint4*>(y + (row + t) * F + fb + c * V) = Pairs<T>::pack(acc);
-#pragma unroll
-        for (int j = Hl - 1; j > 0; --j) {
-#pragma unroll
-            for (int p = 0; p < P; ++p) win[j][p] = win[j - 1][p];
-        }
-        if (Hl > 0) {
-#pragma unroll
-            for (int p = 0; p < P; ++p) win[0][p] = cur[p];
-        }
     }
+    cp_async_wait<0>();                         // nothing left in flight when the thread exits
 }
 
 template <typename T>
 kda_status_t launch_typed(const void* x, const void* w, const int32_t* seg, void* y, int64_t B,
                           int64_t T_len, int64_t F, int32_t K, cudaStream_t stream) {
-    const int64_t tiles = ceil_div(T_len, kTok);
-    const int64_t gx = B * tiles;
     const int64_t gy = ceil_div(F * int64_t(sizeof(T)), kTileBytes);
+    // spans of whole tiles, about kConvCtasPerSm CTAs per SM over all (row, feature block)
+    const int64_t target = int64_t(kConvCtasPerSm) * sm_count();
+    const int64_t pairs = B * gy;
+    int64_t spans = ceil_div(target, pairs > 0 ? pairs : 1);
+    int64_t span = ceil_div(ceil_div(T_len, spans), int64_t(kTok)) * kTok;
+    if (span < kTok) span = kTok;
+    spans = ceil_div(T_len, span);
+    const int64_t gx = B * spans;
     if (gx > 2147483647LL || gy > 65535) return KDA_ERR_UNSUPPORTED;
     const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 1u);
     const T* xp = static_cast<const T*>(x);
@@ -214,10 +248,10 @@ kda_status_t launch_typed(const void* x, const void* w, const int32_t* seg, void
     case KK: {                                                                                 \
         static cudaError_t attr = cudaFuncSetAttribute(                                        \
             short_conv_kernel<T, KK>, cudaFuncAttributeMaxDynamicSharedMemorySize,              \
-            conv_smem_bytes<KK>());                                                            \
+            conv_smem_bytes());                                                                \
         if (attr != cudaSuccess) return KDA_ERR_CUDA;                                          \
-        short_conv_kernel<T, KK><<<grid, kConvThreads, conv_smem_bytes<KK>(), stream>>>(       \
-            xp, wp, seg, yp, T_len, F, tiles);                                                 \
+        short_conv_kernel<T, KK><<<grid, kConvThreads, conv_smem_bytes(), stream>>>(           \
+            xp, wp, seg, yp, T_len, F, span, spans);                                           \
         break;                                                                                 \
     }
         KDA_CONV_CASE(1) KDA_CONV_CASE(2) KDA_CONV_CASE(3) KDA_CONV_CASE(4)

@@ -12,9 +12,11 @@
 // thread owns a contiguous run of 32 ids, read with eight 16-byte loads (one
 // round trip per tile), and takes the previous token's id from its own run or,
 // for its first token, from the neighbouring thread (a shuffle, or shared memory
-// across warps and tiles). Each thread ranks its starts with a block-wide
-// exclusive scan of per-thread counts, so the k-th start lands in cu_seqlens[k]
-// by a direct scatter in token order: no scratch memory and no second pass.
+// across warps and tiles). Starts are found as bitmasks over the run (real tokens,
+// id changes, and the run's one possible row start when T >= 32). Each thread ranks
+// its starts with a block-wide exclusive scan of per-thread counts, so the k-th start
+// lands in cu_seqlens[k] by a direct scatter in token order: no scratch memory and no
+// second pass.
 #include "kda_common.cuh"
 
 namespace kda {
@@ -26,8 +28,8 @@ constexpr int kWarps = kThreads / 32;
 constexpr int64_t kTile = int64_t(kThreads) * kRun;
 
 __global__ void __launch_bounds__(kThreads, 1)
-segids_to_cu_seqlens_kernel(const int32_t* __restrict__ seg, int64_t N, RowStartTest row_start,
-                            int32_t max_segs, int32_t* __restrict__ cu,
+segids_to_cu_seqlens_kernel(const int32_t* __restrict__ seg, int64_t N, int64_t T,
+                            RowStartTest row_start, int32_t max_segs, int32_t* __restrict__ cu,
                             int32_t* __restrict__ n_segs_out) {
     __shared__ int warp_sum[kWarps];
     __shared__ int32_t warp_last_id[kWarps];       // last id of each warp's last thread
@@ -61,15 +63,27 @@ segids_to_cu_seqlens_kernel(const int32_t* __restrict__ seg, int64_t N, RowStart
         if (lane == 31) warp_last_id[warp] = id[kRun - 1];
         __syncthreads();                            // also orders carry_id from the last tile
         if (lane == 0) prev = (warp == 0) ? carry_id : warp_last_id[warp - 1];
-        unsigned mask = 0;
+        // bit i: token p0 + i is real / differs from its predecessor / starts a row (ids
+        // past N were read as 0, so they are not real)
+        unsigned realm = 0, diffm = 0, rowm = 0;
 #pragma unroll
         for (int i = 0; i < kRun; ++i) {
-            const int64_t p = p0 + i;
             const int32_t before = (i == 0) ? prev : id[i - 1];
-            const bool real = p < N && id[i] != 0;
-            if (real) last_real_end = p + 1;
-            const bool st = real && (row_start(p) || before != id[i]);
-            mask |= unsigned(st) << i;
+            realm |= unsigned(id[i] != 0) << i;
+            diffm |= unsigned(before != id[i]) << i;
+        }
+        if (T >= kRun) {                            // at most one row start in the run
+            const int64_t rem = p0 % T;
+            const int64_t o = rem ? T - rem : 0;
+            if (o < kRun) rowm = 1u << o;
+        } else {
+#pragma unroll
+            for (int i = 0; i < kRun; ++i) rowm |= unsigned(row_start(p0 + i)) << i;
+        }
+        unsigned mask = realm & (diffm | rowm);
+        if (realm) {
+            const int64_t e = p0 + kRun - __clz(realm);   // one past the run's last real token
+            last_real_end = e > last_real_end ? e : last_real_end;
         }
         // block exclusive scan of the per-thread start counts
         const int cnt = __popc(mask);
@@ -142,6 +156,6 @@ kda_status_t kda_launch_segids_to_cu_seqlens(const int32_t* seg, int64_t B, int6
                                              int32_t max_segs, int32_t* cu, int32_t* n_segs,
                                              cudaStream_t stream) {
     kda::segids_to_cu_seqlens_kernel<<<1, kda::kThreads, 0, stream>>>(
-        seg, B * T, kda::RowStartTest::make(T), max_segs, cu, n_segs);
+        seg, B * T, T, kda::RowStartTest::make(T), max_segs, cu, n_segs);
     return kda::launch_status();
 }

@@ -61,6 +61,9 @@ def _load():
             lib.oracle_kda_fwd.argtypes = [dp, dp, dp, dp, dp, ip, i64, i64, i64, i64, i64,
                                            ctypes.c_double, dp, ctypes.c_int]
             lib.oracle_kda_fwd.restype = ctypes.c_int
+            lib.oracle_kda_fwd_state.argtypes = [dp, dp, dp, dp, dp, ip, i64, i64, i64, i64, i64,
+                                                 ctypes.c_double, dp, dp, i64, dp, ctypes.c_int]
+            lib.oracle_kda_fwd_state.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -137,6 +140,24 @@ def kda_fwd(q, k, v, g, beta, seg=None, B: int | None = None, T: int | None = No
     seg: [B, T] int32 or None (each row one segment). Returns o [B*T, H, Dv]
     (float64 unless out_dtype says otherwise).
     """
+    o, _ = kda_fwd_state(q, k, v, g, beta, seg, B=B, T=T, scale=scale, n_threads=n_threads,
+                         out_dtype=out_dtype)
+    return o
+
+
+def kda_fwd_state(q, k, v, g, beta, seg=None, B: int | None = None, T: int | None = None,
+                  scale: float = 1.0, initial_state=None, n_state: int = 0,
+                  want_final: bool = False, n_threads: int | None = None,
+                  out_dtype=torch.float64):
+    """The recurrence with per-segment state in and out (RFC-0026, the initial_state /
+    output_final_state kwargs of the chunk_kda call).
+
+    Segment r (counted in flattened token order, as in cu_seqlens) starts from
+    initial_state[r] ([n_state, H, Dk, Dv]) instead of zero when r < n_state; with
+    want_final, final[r] is its state after its last token (zero for r >= the
+    segment count). Returns (o, final or None), both float64 unless out_dtype says
+    otherwise.
+    """
     qa, ka, va, ga = (_np(t, np.float64) for t in (q, k, v, g))
     ba = _np(beta, np.float64)
     if seg is not None:
@@ -157,9 +178,15 @@ def kda_fwd(q, k, v, g, beta, seg=None, B: int | None = None, T: int | None = No
     va = va.reshape(N, H, Dv)
     ba = ba.reshape(N, H)
     o = np.zeros((N, H, Dv), dtype=np.float64)
+    ia = None
+    if initial_state is not None:
+        ia = _np(initial_state, np.float64).reshape(n_state, H, Dk, Dv)
+    fa = np.zeros((n_state, H, Dk, Dv), dtype=np.float64) if want_final else None
     nt = default_threads() if n_threads is None else n_threads
-    rc = _load().oracle_kda_fwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), _ptr(ba), _ptr(sa),
-                                B, T, H, Dk, Dv, float(scale), _ptr(o), int(nt))
+    rc = _load().oracle_kda_fwd_state(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), _ptr(ba),
+                                      _ptr(sa), B, T, H, Dk, Dv, float(scale), _ptr(ia),
+                                      _ptr(fa), int(n_state), _ptr(o), int(nt))
     if rc != 0:
-        raise ValueError("oracle_kda_fwd: bad arguments")
-    return torch.from_numpy(o).to(out_dtype)
+        raise ValueError("oracle_kda_fwd_state: bad arguments")
+    fin = torch.from_numpy(fa).to(out_dtype) if fa is not None else None
+    return torch.from_numpy(o).to(out_dtype), fin

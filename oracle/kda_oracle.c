@@ -146,17 +146,26 @@ typedef struct {
     int64_t B, T, H, Dk, Dv;
     double scale;
     double *o;
-    /* work units: (row, head, first token, one-past-last token) */
+    /* per-segment state, [n_state, H, Dk, Dv]; either may be NULL */
+    const double *init;
+    double *fin;
+    int64_t n_state;
+    /* work units: (row, head, first token, one-past-last token, segment rank) */
     const int64_t *units;
     int64_t n_units;
     int64_t next; /* shared counter */
 } kda_job_t;
 
 static void run_unit(const kda_job_t *J, int64_t b, int64_t h, int64_t t0, int64_t t1,
-                     double *S)
+                     int64_t r, double *S)
 {
     const int64_t H = J->H, Dk = J->Dk, Dv = J->Dv;
-    memset(S, 0, sizeof(double) * (size_t)(Dk * Dv));
+    /* the segment's state before its first token: its initial state, or zero */
+    const int64_t slot = (r * H + h) * Dk * Dv;
+    if (J->init && r < J->n_state)
+        memcpy(S, J->init + slot, sizeof(double) * (size_t)(Dk * Dv));
+    else
+        memset(S, 0, sizeof(double) * (size_t)(Dk * Dv));
     for (int64_t t = t0; t < t1; ++t) {
         const int64_t p = b * J->T + t;
         const double *qt = J->q + (p * H + h) * Dk;
@@ -179,6 +188,9 @@ static void run_unit(const kda_job_t *J, int64_t b, int64_t h, int64_t t0, int64
             ot[j] = J->scale * acc;
         }
     }
+    /* the segment's state after its last token */
+    if (J->fin && r < J->n_state)
+        memcpy(J->fin + slot, S, sizeof(double) * (size_t)(Dk * Dv));
 }
 
 static void *kda_worker(void *arg)
@@ -191,8 +203,8 @@ static void *kda_worker(void *arg)
         const int64_t u = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
         if (u >= J->n_units)
             break;
-        const int64_t *U = J->units + 4 * u;
-        run_unit(J, U[0], U[1], U[2], U[3], S);
+        const int64_t *U = J->units + 5 * u;
+        run_unit(J, U[0], U[1], U[2], U[3], U[4], S);
     }
     free(S);
     return NULL;
@@ -202,13 +214,22 @@ static void *kda_worker(void *arg)
  * Splits every row into its segments (maximal runs of equal non-zero ids,
  * cut at row starts), zeroes o, and runs one independent recurrence per
  * (segment, head) on `n_threads` threads. Starting each segment from S = 0
- * is exactly the reset rule above. Returns 0, or -1 on bad arguments.
+ * is exactly the reset rule above.
+ *
+ * Per-segment state ([RFC-0026] 方案, the kernel kwargs initial_state and
+ * output_final_state of the FLA chunk_kda call; shapes [n_segments, H, Dk, Dv]):
+ * segment r, counted in flattened token order, starts from init[r] instead of
+ * zero when init is given and r < n_state, and its state after its last token
+ * is written to fin[r] when fin is given and r < n_state. With init = NULL this
+ * is the reset rule above. Returns 0, or -1 on bad arguments.
  */
-int oracle_kda_fwd(const double *q, const double *k, const double *v, const double *g,
-                   const double *beta, const int32_t *seg, int64_t B, int64_t T, int64_t H,
-                   int64_t Dk, int64_t Dv, double scale, double *o, int n_threads)
+int oracle_kda_fwd_state(const double *q, const double *k, const double *v, const double *g,
+                         const double *beta, const int32_t *seg, int64_t B, int64_t T, int64_t H,
+                         int64_t Dk, int64_t Dv, double scale, const double *init, double *fin,
+                         int64_t n_state, double *o, int n_threads)
 {
-    if (!q || !k || !v || !g || !beta || !o || B < 0 || T < 0 || H < 1 || Dk < 1 || Dv < 1)
+    if (!q || !k || !v || !g || !beta || !o || B < 0 || T < 0 || H < 1 || Dk < 1 || Dv < 1 ||
+        n_state < 0)
         return -1;
     const int64_t N = B * T;
     memset(o, 0, sizeof(double) * (size_t)(N * H * Dv));
@@ -221,10 +242,11 @@ int oracle_kda_fwd(const double *q, const double *k, const double *v, const doub
             if (s != 0 && (t == 0 || (seg ? seg[p - 1] : 1) != s))
                 n_seg += 1;
         }
-    int64_t *units = (int64_t *)malloc(sizeof(int64_t) * 4 * (size_t)(n_seg * H + 1));
+    int64_t *units = (int64_t *)malloc(sizeof(int64_t) * 5 * (size_t)(n_seg * H + 1));
     if (!units)
         return -1;
     int64_t n_units = 0;
+    int64_t rank = 0; /* segments in flattened token order */
     for (int64_t b = 0; b < B; ++b) {
         int64_t t = 0;
         while (t < T) {
@@ -238,16 +260,19 @@ int oracle_kda_fwd(const double *q, const double *k, const double *v, const doub
             while (e < T && (seg ? seg[b * T + e] : 1) == s)
                 ++e;
             for (int64_t h = 0; h < H; ++h) {
-                units[4 * n_units + 0] = b;
-                units[4 * n_units + 1] = h;
-                units[4 * n_units + 2] = t;
-                units[4 * n_units + 3] = e;
+                units[5 * n_units + 0] = b;
+                units[5 * n_units + 1] = h;
+                units[5 * n_units + 2] = t;
+                units[5 * n_units + 3] = e;
+                units[5 * n_units + 4] = rank;
                 ++n_units;
             }
+            ++rank;
             t = e;
         }
     }
-    kda_job_t J = {q, k, v, g, beta, seg, B, T, H, Dk, Dv, scale, o, units, n_units, 0};
+    kda_job_t J = {q, k, v, g, beta, seg, B, T, H, Dk, Dv, scale, o,
+                   init, fin, n_state, units, n_units, 0};
     if (n_threads < 1)
         n_threads = 1;
     if (n_threads > 256)
@@ -267,4 +292,13 @@ int oracle_kda_fwd(const double *q, const double *k, const double *v, const doub
     }
     free(units);
     return 0;
+}
+
+/* The recurrence with every segment starting from zero and no state written. */
+int oracle_kda_fwd(const double *q, const double *k, const double *v, const double *g,
+                   const double *beta, const int32_t *seg, int64_t B, int64_t T, int64_t H,
+                   int64_t Dk, int64_t Dv, double scale, double *o, int n_threads)
+{
+    return oracle_kda_fwd_state(q, k, v, g, beta, seg, B, T, H, Dk, Dv, scale, NULL, NULL, 0, o,
+                                n_threads);
 }

@@ -27,6 +27,9 @@ MUTATIONS = {
                           "const double *gt = J->g + ((p > 0 ? p - 1 : p) * H + h) * Dk;"),
     "no_reset_between_docs": ("while (e < T && (seg ? seg[b * T + e] : 1) == s)",
                               "while (e < T && (seg ? seg[b * T + e] : 1) != 0)"),
+    # per-segment state
+    "initial_state_ignored": ("if (J->init && r < J->n_state)", "if (0 && J->init && r < J->n_state)"),
+    "state_rank_off_by_one": ("units[5 * n_units + 4] = rank;", "units[5 * n_units + 4] = rank + 1;"),
     # conv
     "conv_tap_forward": ("const int64_t s = t - j;", "const int64_t s = t - (K - 1 - j);"),
     "conv_no_mask": ("if (seg && seg[b * T + s] != seg[b * T + t])", "if (0)"),
@@ -59,10 +62,13 @@ def _pins_pass(monkeypatch, so_path) -> bool:
     lib.oracle_short_conv.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
     lib.oracle_kda_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                    ctypes.c_double, vp, ctypes.c_int]
+    lib.oracle_kda_fwd_state.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                         ctypes.c_double, vp, vp, i64, vp, ctypes.c_int]
     monkeypatch.setattr(oracle, "_lib", lib)
     import tests.test_oracle_cu_seqlens as tc
     import tests.test_oracle_conv as tv
     import tests.test_oracle_kda as tk
+    import tests.test_oracle_state as ts
     golden = os.path.join(os.path.dirname(tc.__file__), "golden")
     checks = [
         lambda: tc.test_worked_examples(golden),
@@ -77,6 +83,9 @@ def _pins_pass(monkeypatch, so_path) -> bool:
         lambda: tk.test_zero_decay_is_causal_linear_attention(),
         lambda: tk.test_scalar_channel_is_first_order_filter(),
         lambda: tk.test_length_one_documents(),
+        lambda: ts.test_closed_forms_bruteforce(),
+        lambda: ts.test_chaining_identity(),
+        lambda: ts.test_state_slots_beyond_n_state_and_ranks(),
     ]
     for c in checks:
         try:

@@ -329,6 +329,30 @@ def run_gb300(args):
     if int(status.item()) != 0:
         print(f"warning: device status {int(status.item()):#x}", file=sys.stderr)
 
+    # ---- per-segment state in and out (kda_chunk_fwd_varlen_state), timed apart ----
+    n_state = int(nseg.item())
+    st_gen = torch.Generator(device=dev).manual_seed(11)
+    init = torch.randn(n_state, H, wl.d_qk, wl.d_v, device=dev, generator=st_gen) * 0.1
+    state_ms = None
+    if n_state > 0:
+        def state_call():
+            kda.kda_chunk_fwd_varlen_state(kin.q, kin.k, kin.v, kin.g, kin.beta, seg, B=wl.B,
+                                           T=wl.T, initial_state=init, output_final_state=True,
+                                           out=o, workspace=work, status=status)
+
+        for _ in range(2):
+            state_call()
+        torch.cuda.synchronize()
+        sa = torch.cuda.Event(enable_timing=True)
+        sb = torch.cuda.Event(enable_timing=True)
+        n_rep = 5
+        sa.record(stream)
+        for _ in range(n_rep):
+            state_call()
+        sb.record(stream)
+        torch.cuda.synchronize()
+        state_ms = sa.elapsed_time(sb) / n_rep
+
     # ---- e2e through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
@@ -442,7 +466,10 @@ def run_gb300(args):
             for name, ms_, nbytes in (
                 ("kda_segids_to_cu_seqlens", seg_ms, 4 * N),
                 ("kda_short_conv_varlen", conv_ms, 2 * N * wl.F * convs[0].x.element_size()),
-                ("kda_chunk_fwd_varlen", chunk_ms, bytes_launch))
+                ("kda_chunk_fwd_varlen", chunk_ms, bytes_launch),
+                ("kda_chunk_fwd_varlen_state", state_ms,
+                 bytes_launch + 2 * n_state * H * wl.d_qk * wl.d_v * 4))
+            if ms_ is not None
         },
         "real_tokens_per_s": real_tokens * ws / (ms / 1e3),
         "gpu_launches": args.steps * 7,

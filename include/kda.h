@@ -156,6 +156,40 @@ kda_status_t kda_chunk_fwd_varlen(const void *q, const void *k, const void *v, c
                                   kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd_varlen_state -- kda_chunk_fwd_varlen with per-segment recurrent
+ * state in and out: the initial_state and output_final_state kwargs that
+ * [RFC-0026] passes to the chunked KDA call, one state per packed sequence.
+ *
+ * Segment r is the r-th segment of the flattened [B*T] sequence in token order
+ * (the r-th entry of cu_seqlens; rows first, padding is no segment, and with
+ * segment_ids == NULL segment r is row r). For r < n_state:
+ *   initial_state  device fp32 [n_state, H, d_qk, d_v] or NULL: segment r starts
+ *                  from initial_state[r] instead of 0 (rows are key channels:
+ *                  S[i][j], i < d_qk, j < d_v);
+ *   final_state    device fp32 [n_state, H, d_qk, d_v] or NULL: receives segment
+ *                  r's state after its last token. Slots r >= the segment count
+ *                  are left untouched.
+ * Segments r >= n_state start from 0 and are not written out. Both arrays are
+ * owned by the caller, 16-byte aligned, and must not overlap.
+ *
+ * The other arguments are those of kda_chunk_fwd_varlen, with the same
+ * workspace size. Every dtype runs the token recurrence in fp32 arithmetic
+ * (one walk per segment and head); the tensor-core chunked form does not carry
+ * per-segment state yet.
+ *
+ * Returns KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE or
+ * KDA_ERR_CUDA. Calls that share a workspace must not overlap in time.
+ */
+kda_status_t kda_chunk_fwd_varlen_state(const void *q, const void *k, const void *v,
+                                        const void *g, const void *beta,
+                                        const int32_t *segment_ids, int64_t B, int64_t T,
+                                        int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                        kda_dtype_t dtype, kda_dtype_t out_dtype, void *o,
+                                        const float *initial_state, float *final_state,
+                                        int64_t n_state, void *workspace, size_t workspace_bytes,
+                                        uint32_t *status_dev, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_varlen_noalloc -- kda_chunk_fwd_varlen for callers that cannot
  * allocate device memory. The pages have no counterpart: this is a calling
  * convention of this library, not part of the method.

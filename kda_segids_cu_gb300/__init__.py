@@ -61,6 +61,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                          ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, vp,
                                          ctypes.c_size_t, u32p, vp]
     lib.kda_chunk_fwd_varlen.restype = ctypes.c_int
+    lib.kda_chunk_fwd_varlen_state.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32,
+                                               ctypes.c_float, ctypes.c_int, ctypes.c_int, vp,
+                                               vp, vp, i64, vp, ctypes.c_size_t, u32p, vp]
+    lib.kda_chunk_fwd_varlen_state.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -148,17 +152,8 @@ def chunk_fwd_workspace_bytes(B: int, T: int, H: int, d_qk: int, d_v: int, dtype
                                                                   _dtype_code(dtype)))
 
 
-def kda_chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
-                         beta: torch.Tensor, segment_ids: torch.Tensor | None = None,
-                         scale: float = 1.0, B: int | None = None, T: int | None = None,
-                         stream=None, out: torch.Tensor | None = None,
-                         workspace: torch.Tensor | None = None,
-                         status: torch.Tensor | None = None,
-                         out_dtype: torch.dtype | None = None) -> torch.Tensor:
-    """Packed KDA forward. q, k, g: [B, T, H, Dk], [1, B*T, H, Dk] or [B*T, H, Dk];
-    v like q with Dv; beta [..., H]; segment_ids int32 [B, T] or None.
-    Returns o shaped like v, of `out_dtype` (default: the input dtype; float32
-    is also accepted)."""
+def _chunk_args(q, k, v, g, beta, segment_ids, B, T, out, workspace, out_dtype):
+    """Checks and marshals the arguments the chunk entry points share."""
     q, k, v, g, beta = (_dev(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (g, "g"),
                                                  (beta, "beta")))
     H, Dk = q.shape[-2], q.shape[-1]
@@ -194,6 +189,22 @@ def kda_chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: t
     need = chunk_fwd_workspace_bytes(B, T, H, Dk, Dv, q.dtype)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    return q, k, v, g, beta, seg, B, T, H, Dk, Dv, dt, odt, o, workspace
+
+
+def kda_chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                         beta: torch.Tensor, segment_ids: torch.Tensor | None = None,
+                         scale: float = 1.0, B: int | None = None, T: int | None = None,
+                         stream=None, out: torch.Tensor | None = None,
+                         workspace: torch.Tensor | None = None,
+                         status: torch.Tensor | None = None,
+                         out_dtype: torch.dtype | None = None) -> torch.Tensor:
+    """Packed KDA forward. q, k, g: [B, T, H, Dk], [1, B*T, H, Dk] or [B*T, H, Dk];
+    v like q with Dv; beta [..., H]; segment_ids int32 [B, T] or None.
+    Returns o shaped like v, of `out_dtype` (default: the input dtype; float32
+    is also accepted)."""
+    q, k, v, g, beta, seg, B, T, H, Dk, Dv, dt, odt, o, workspace = _chunk_args(
+        q, k, v, g, beta, segment_ids, B, T, out, workspace, out_dtype)
     _check("kda_chunk_fwd_varlen",
            load_library().kda_chunk_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                                _ptr(seg), B, T, H, Dk, Dv, float(scale), dt,
@@ -202,6 +213,42 @@ def kda_chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: t
     return o
 
 
+def kda_chunk_fwd_varlen_state(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                               g: torch.Tensor, beta: torch.Tensor,
+                               segment_ids: torch.Tensor | None = None, scale: float = 1.0,
+                               B: int | None = None, T: int | None = None,
+                               initial_state: torch.Tensor | None = None,
+                               output_final_state: bool = False, n_state: int | None = None,
+                               stream=None, out: torch.Tensor | None = None,
+                               workspace: torch.Tensor | None = None,
+                               status: torch.Tensor | None = None,
+                               out_dtype: torch.dtype | None = None):
+    """kda_chunk_fwd_varlen with per-segment state: segment r (flattened token order,
+    as in cu_seqlens) starts from initial_state[r] ([n_state, H, Dk, Dv] float32) and,
+    with output_final_state, its state after its last token is returned in
+    final[r]. n_state defaults to initial_state's first dimension (else 0).
+    Returns (o, final or None)."""
+    q, k, v, g, beta, seg, B, T, H, Dk, Dv, dt, odt, o, workspace = _chunk_args(
+        q, k, v, g, beta, segment_ids, B, T, out, workspace, out_dtype)
+    if n_state is None:
+        n_state = initial_state.shape[0] if initial_state is not None else 0
+    init = None
+    if initial_state is not None:
+        init = _dev(initial_state, "initial_state")
+        if init.dtype != torch.float32 or init.numel() != n_state * H * Dk * Dv:
+            raise ValueError("initial_state must be float32 [n_state, H, Dk, Dv]")
+    fin = None
+    if output_final_state:
+        fin = torch.zeros((n_state, H, Dk, Dv), dtype=torch.float32, device=q.device)
+    _check("kda_chunk_fwd_varlen_state",
+           load_library().kda_chunk_fwd_varlen_state(
+               _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(seg), B, T, H, Dk, Dv,
+               float(scale), dt, odt, _ptr(o), _ptr(init), _ptr(fin), int(n_state),
+               _ptr(workspace), workspace.numel(), _ptr(status), _stream_ptr(stream)))
+    return o, fin
+
+
 __all__ = ["kda_segids_to_cu_seqlens", "kda_short_conv_varlen", "kda_chunk_fwd_varlen",
+           "kda_chunk_fwd_varlen_state",
            "chunk_fwd_workspace_bytes", "load_library", "header_functions", "KdaError",
            "KDA_DEV_DECAY_RANGE"]

@@ -9,6 +9,11 @@ kda_status_t launch_recurrent(const void* q, const void* k, const void* v, const
                               const void* beta, const int32_t* seg, int64_t B, int64_t T,
                               int32_t H, int32_t D, float scale, kda_dtype_t dtype,
                               kda_dtype_t out_dtype, void* o, void* ws, cudaStream_t stream);
+kda_status_t launch_recurrent_state(const void* q, const void* k, const void* v, const void* g,
+                                    const void* beta, const int32_t* seg, int64_t B, int64_t T_len,
+                                    int32_t H, int32_t D, float scale, kda_dtype_t dtype,
+                                    kda_dtype_t out_dtype, void* o, void* ws, const float* init,
+                                    float* fin, int64_t n_state, cudaStream_t stream);
 kda_status_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* g,
                              const void* beta, const int32_t* seg, int64_t B, int64_t T,
                              int32_t H, int32_t D, float scale, kda_dtype_t out_dtype, void* o,
@@ -105,6 +110,38 @@ kda_status_t kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, c
                                     out_dtype, o, workspace, status_dev, st);
     return kda::launch_recurrent(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale, dtype,
                                  out_dtype, o, workspace, st);
+}
+
+kda_status_t kda_chunk_fwd_varlen_state(const void* q, const void* k, const void* v,
+                                        const void* g, const void* beta,
+                                        const int32_t* segment_ids, int64_t B, int64_t T,
+                                        int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                        kda_dtype_t dtype, kda_dtype_t out_dtype, void* o,
+                                        const float* initial_state, float* final_state,
+                                        int64_t n_state, void* workspace, size_t workspace_bytes,
+                                        uint32_t* status_dev, kda_stream_t stream) {
+    if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !valid_dtype(out_dtype) || !token_count_ok(B, T) || H < 1 ||
+        d_qk < 1 || d_v < 1 || n_state < 0)
+        return KDA_ERR_INVALID_ARG;
+    if (out_dtype != dtype && out_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return KDA_ERR_UNSUPPORTED;
+    if (int64_t(H) * d_qk > 65536) return KDA_ERR_UNSUPPORTED;
+    if (n_state > (int64_t(1) << 40) / (int64_t(H) * d_qk * d_v)) return KDA_ERR_UNSUPPORTED;
+    const void* ptrs[] = {q, k, v, g, beta, o};
+    for (const void* p : ptrs)
+        if (!kda::aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if ((initial_state && !kda::aligned(initial_state, 16)) ||
+        (final_state && !kda::aligned(final_state, 16)))
+        return KDA_ERR_INVALID_ARG;
+    if (segment_ids && !kda::aligned(segment_ids, 4)) return KDA_ERR_INVALID_ARG;
+    if (status_dev && !kda::aligned(status_dev, 4)) return KDA_ERR_INVALID_ARG;
+    const size_t need = kda_chunk_fwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
+    if (!workspace || workspace_bytes < need || !kda::aligned(workspace, 256))
+        return KDA_ERR_WORKSPACE;
+    return kda::launch_recurrent_state(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale, dtype,
+                                       out_dtype, o, workspace, initial_state, final_state,
+                                       n_state, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -18,6 +18,12 @@
 // staged kWin at a time in shared memory as fp32 (exp(g) and beta*k
 // precomputed there), and the two half-column partial read-outs are summed
 // once per window.
+//
+// Per-segment state (the initial_state / output_final_state kwargs that [RFC-0026]
+// passes to the chunked call): a unit of segment r starts from init[r] instead of
+// zero and stores its state after the last token to fin[r] (both [n_state, H, D, D]
+// fp32, row = key channel), when given and r < n_state; r is the segment's rank in
+// flattened token order, as in cu_seqlens.
 #include "kda_common.cuh"
 
 namespace kda {
@@ -119,7 +125,8 @@ __global__ void __launch_bounds__(2 * D)
 recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                  const T* __restrict__ g, const T* __restrict__ beta, int32_t H, float scale,
                  const int32_t* __restrict__ seg_start, const int32_t* __restrict__ seg_end,
-                 const int32_t* __restrict__ counters, To* __restrict__ o) {
+                 const int32_t* __restrict__ counters, To* __restrict__ o,
+                 const float* __restrict__ init, float* __restrict__ fin, int64_t n_state) {
     constexpr int R = D / 2;              // state rows per thread
     constexpr int kWin = Win<D>::value;   // tokens staged per window (48 KB of smem)
     __shared__ float sq[kWin][D];
@@ -139,8 +146,11 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
         const int64_t p0 = seg_start[s_idx];
         const int64_t p1 = seg_end[s_idx];
         float S[R];
+        // this thread's rows half*R .. +R-1 of column c in the segment's state slot
+        const int64_t slot = ((s_idx * H + h) * D + half * R) * D + c;
+        const bool has_slot = s_idx < n_state;
 #pragma unroll
-        for (int r = 0; r < R; ++r) S[r] = 0.f;
+        for (int r = 0; r < R; ++r) S[r] = (init && has_slot) ? init[slot + int64_t(r) * D] : 0.f;
 
         for (int64_t pw = p0; pw < p1; pw += kWin) {
             const int nw = int((p1 - pw < kWin) ? p1 - pw : int64_t(kWin));
@@ -173,6 +183,10 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                 o[row * D + j] = from_f32<To>(scale * (part[0][w][j] + part[1][w][j]));
             }
         }
+        if (fin && has_slot) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) fin[slot + int64_t(r) * D] = S[r];
+        }
     }
 }
 
@@ -187,8 +201,8 @@ template <typename T, typename To>
 static kda_status_t launch_recurrent_typed(const void* q, const void* k, const void* v,
                                            const void* g, const void* beta, const int32_t* seg,
                                            int64_t B, int64_t T_len, int32_t H, int32_t D,
-                                           float scale, void* o, void* ws,
-                                           cudaStream_t stream) {
+                                           float scale, void* o, void* ws, const float* init,
+                                           float* fin, int64_t n_state, cudaStream_t stream) {
     const int64_t N = B * T_len;
     int32_t* seg_start = static_cast<int32_t*>(ws);
     int32_t* seg_end = seg_start + N;
@@ -211,27 +225,39 @@ static kda_status_t launch_recurrent_typed(const void* q, const void* k, const v
     To* op = static_cast<To*>(o);
     if (D == 64)
         recurrent_kernel<T, To, 64><<<blocks, 128, 0, stream>>>(qp, kp, vp, gp, bp, H, scale,
-                                                                seg_start, seg_end, counters, op);
+                                                                seg_start, seg_end, counters, op,
+                                                                init, fin, n_state);
     else
         recurrent_kernel<T, To, 128><<<blocks, 256, 0, stream>>>(qp, kp, vp, gp, bp, H, scale,
-                                                                 seg_start, seg_end, counters, op);
+                                                                 seg_start, seg_end, counters, op,
+                                                                 init, fin, n_state);
     return launch_status();
+}
+
+kda_status_t launch_recurrent_state(const void* q, const void* k, const void* v, const void* g,
+                                    const void* beta, const int32_t* seg, int64_t B, int64_t T_len,
+                                    int32_t H, int32_t D, float scale, kda_dtype_t dtype,
+                                    kda_dtype_t out_dtype, void* o, void* ws, const float* init,
+                                    float* fin, int64_t n_state, cudaStream_t stream) {
+    if (dtype == KDA_BF16) {
+        if (out_dtype == KDA_F32)
+            return launch_recurrent_typed<__nv_bfloat16, float>(q, k, v, g, beta, seg, B, T_len,
+                                                                H, D, scale, o, ws, init, fin,
+                                                                n_state, stream);
+        return launch_recurrent_typed<__nv_bfloat16, __nv_bfloat16>(q, k, v, g, beta, seg, B,
+                                                                    T_len, H, D, scale, o, ws,
+                                                                    init, fin, n_state, stream);
+    }
+    return launch_recurrent_typed<float, float>(q, k, v, g, beta, seg, B, T_len, H, D, scale, o,
+                                                ws, init, fin, n_state, stream);
 }
 
 kda_status_t launch_recurrent(const void* q, const void* k, const void* v, const void* g,
                               const void* beta, const int32_t* seg, int64_t B, int64_t T_len,
                               int32_t H, int32_t D, float scale, kda_dtype_t dtype,
                               kda_dtype_t out_dtype, void* o, void* ws, cudaStream_t stream) {
-    if (dtype == KDA_BF16) {
-        if (out_dtype == KDA_F32)
-            return launch_recurrent_typed<__nv_bfloat16, float>(q, k, v, g, beta, seg, B, T_len,
-                                                                H, D, scale, o, ws, stream);
-        return launch_recurrent_typed<__nv_bfloat16, __nv_bfloat16>(q, k, v, g, beta, seg, B,
-                                                                    T_len, H, D, scale, o, ws,
-                                                                    stream);
-    }
-    return launch_recurrent_typed<float, float>(q, k, v, g, beta, seg, B, T_len, H, D, scale, o,
-                                                ws, stream);
+    return launch_recurrent_state(q, k, v, g, beta, seg, B, T_len, H, D, scale, dtype, out_dtype,
+                                  o, ws, nullptr, nullptr, 0, stream);
 }
 
 }  // namespace kda

@@ -88,3 +88,28 @@ def test_chunk_rejects_invalid_arguments(lib):
     assert call(ws_bytes=ws - 1) == -4
     assert call(ws=ctypes.c_void_p(4096 + 16)) == -4          # workspace must be 256-aligned
     assert call(status=ODD) == -1
+
+
+def test_chunk_state_rejects_invalid_arguments(lib):
+    f = lib.kda_chunk_fwd_varlen_state
+    ws = lib.kda_chunk_fwd_varlen_workspace_size(1, 64, 2, 64, 64, kda.KDA_BF16)
+    args = [FAKE] * 5 + [None, 1, 64, 2, 64, 64, ctypes.c_float(1.0), kda.KDA_BF16, kda.KDA_BF16,
+                         FAKE, FAKE, FAKE, 3, FAKE, ws, None, None]
+
+    def call(**over):
+        a = list(args)
+        idx = {"q": 0, "B": 6, "dk": 9, "dv": 10, "o": 14, "init": 15, "fin": 16, "n_state": 17,
+               "ws": 18, "ws_bytes": 19}
+        for k, v in over.items():
+            a[idx[k]] = v
+        return f(*a)
+
+    assert call(q=None) == -1
+    assert call(o=None) == -1
+    assert call(B=0) == -1
+    assert call(n_state=-1) == -1
+    assert call(init=ODD) == -1
+    assert call(fin=ODD) == -1
+    assert call(dk=96, dv=96) == -2
+    assert call(ws=None) == -4
+    assert call(ws_bytes=ws - 1) == -4

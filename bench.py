@@ -91,8 +91,8 @@ def chunk_flops_per_token_head(wl: synth.Workload) -> int:
 # `python bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline`. It holds only
 # for the kernel sources it was taken on (SHA-1 over the two files below);
 # after any change to them the bench reports null until a new capture.
-CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "2f337b5aef248419b1fa820d1a49a3d8818211bb",
-                 "read": 558_145_024, "write": 117_566_464}
+CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "72e497cd3dc01b03ae2c67a07e2596f30cdf6e29",
+                 "read": 558_211_840, "write": 118_858_240}
 CHUNK_SOURCES = ("kda_segids_cu_gb300/csrc/kda_chunk_tc.cu", "kda_segids_cu_gb300/csrc/kda_sm100.cuh")
 
 

@@ -13,11 +13,12 @@
 //
 // Work split: a segment-list pass (one CTA, ballot/scan over the ids) writes
 // each segment's [start, end) to the workspace; a persistent grid then walks
-// (segment, head) units. In a unit, 2*D threads hold the D x D state: thread
-// (half, c) keeps rows half*D/2 .. half*D/2 + D/2 - 1 of column c. Tokens are
-// staged kWin at a time in shared memory as fp32 (exp(g) and beta*k
-// precomputed there), and the two half-column partial read-outs are summed
-// once per window.
+// (segment, head) units. In a unit, (D/8)^2 threads hold the D x D state, each an
+// 8 x 8 block (key rows 8 rg .., value columns 8 cg ..) updated with packed fp32x2
+// arithmetic. Tokens are staged kWin at a time in shared memory as fp32 (exp(g)
+// and beta*k precomputed there), the next window's inputs being loaded into
+// registers while the current one is computed. Each token's partial read-outs are
+// summed across the warp's row blocks by shuffles and across warps once per window.
 //
 // Per-segment state (the initial_state / output_final_state kwargs that [RFC-0026]
 // passes to the chunked call): a unit of segment r starts from init[r] instead of
@@ -118,26 +119,52 @@ __global__ void zero_padding_kernel(const int32_t* __restrict__ seg, int64_t N, 
         o[p * row_elems + e] = from_f32<T>(0.f);
 }
 
-template <int D> struct Win { static constexpr int value = D == 64 ? 16 : 8; };
+// Packed fp32 pairs (one f32x2 instruction for two lanes of arithmetic).
+__device__ __forceinline__ float2 rmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 u, v, w;\n\tmov.b64 u, {%2, %3};\n\tmov.b64 v, {%4, %5};\n\t"
+        "mul.rn.f32x2 w, u, v;\n\tmov.b64 {%0, %1}, w;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 rfma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 u, v, w, z;\n\tmov.b64 u, {%2, %3};\n\tmov.b64 v, {%4, %5};\n\t"
+        "mov.b64 w, {%6, %7};\n\tfma.rn.f32x2 z, u, v, w;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+constexpr int kTile = 8;                  // each thread holds an 8 x 8 block of S
+constexpr int kWin = 8;                   // tokens staged per window
+
+template <int D> constexpr int rec_threads() { return (D / kTile) * (D / kTile); }
+template <int D> constexpr int rec_smem_bytes() {
+    // staged q, beta*k, exp(g), v per token, and per-warp partial read-outs
+    return 4 * kWin * D * 4 + (rec_threads<D>() / 32) * kWin * D * 4;
+}
 
 template <typename T, typename To, int D>
-__global__ void __launch_bounds__(2 * D)
+__global__ void __launch_bounds__(rec_threads<D>(), D == 64 ? 8 : 2)
 recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                  const T* __restrict__ g, const T* __restrict__ beta, int32_t H, float scale,
                  const int32_t* __restrict__ seg_start, const int32_t* __restrict__ seg_end,
                  const int32_t* __restrict__ counters, To* __restrict__ o,
                  const float* __restrict__ init, float* __restrict__ fin, int64_t n_state) {
-    constexpr int R = D / 2;              // state rows per thread
-    constexpr int kWin = Win<D>::value;   // tokens staged per window (48 KB of smem)
-    __shared__ float sq[kWin][D];
-    __shared__ float sbk[kWin][D];
-    __shared__ float se[kWin][D];
-    __shared__ float sv[kWin][D];
-    __shared__ float part[2][kWin][D];
+    constexpr int NG = D / kTile;         // row groups = column groups
+    constexpr int NT = NG * NG;
+    constexpr int NW = NT / 32;
+    extern __shared__ __align__(16) float smem[];
+    float* sq = smem;                     // [kWin][D]
+    float* sbk = sq + kWin * D;
+    float* se = sbk + kWin * D;
+    float* sv = se + kWin * D;
+    float* part = sv + kWin * D;          // [NW][kWin][D]
 
     const int tid = threadIdx.x;
-    const int c = tid % D;
-    const int half = tid / D;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int rg = tid / NG, cg = tid % NG;          // key rows 8 rg .., value columns 8 cg ..
     const int64_t n_units = int64_t(counters[0]) * H;
 
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -145,47 +172,117 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
         const int h = int(u % H);
         const int64_t p0 = seg_start[s_idx];
         const int64_t p1 = seg_end[s_idx];
-        float S[R];
-        // this thread's rows half*R .. +R-1 of column c in the segment's state slot
-        const int64_t slot = ((s_idx * H + h) * D + half * R) * D + c;
+        // S[i][jp]: key row 8 rg + i, value columns 8 cg + 2 jp, +1
+        float2 S[kTile][kTile / 2];
+        const int64_t slot = (s_idx * H + h) * int64_t(D) * D;
         const bool has_slot = s_idx < n_state;
 #pragma unroll
-        for (int r = 0; r < R; ++r) S[r] = (init && has_slot) ? init[slot + int64_t(r) * D] : 0.f;
+        for (int i = 0; i < kTile; ++i) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (init && has_slot) {
+                const float* src = init + slot + int64_t(kTile * rg + i) * D + kTile * cg;
+                a = *reinterpret_cast<const float4*>(src);
+                b = *reinterpret_cast<const float4*>(src + 4);
+            }
+            S[i][0] = make_float2(a.x, a.y); S[i][1] = make_float2(a.z, a.w);
+            S[i][2] = make_float2(b.x, b.y); S[i][3] = make_float2(b.z, b.w);
+        }
 
+        // the window's inputs, loaded one window ahead into registers (element
+        // e = tid + m * NT of the window: token e / D, channel e % D)
+        constexpr int PER = kWin * D / NT;
+        float rq[PER], rk[PER], rg_[PER], rv[PER], rb[PER];
+        auto load_window = [&](int64_t pw) {
+            const int nw = int((p1 - pw < kWin) ? p1 - pw : int64_t(kWin));
+#pragma unroll
+            for (int m = 0; m < PER; ++m) {
+                const int e = tid + m * NT, w = e / D, i = e % D;
+                if (pw < p1 && w < nw) {
+                    const int64_t row = (pw + w) * H + h;
+                    rb[m] = to_f32(beta[row]);
+                    rq[m] = to_f32(q[row * D + i]);
+                    rk[m] = to_f32(k[row * D + i]);
+                    rg_[m] = to_f32(g[row * D + i]);
+                    rv[m] = to_f32(v[row * D + i]);
+                }
+            }
+        };
+        load_window(p0);
         for (int64_t pw = p0; pw < p1; pw += kWin) {
             const int nw = int((p1 - pw < kWin) ? p1 - pw : int64_t(kWin));
             __syncthreads();   // previous window fully consumed
-            for (int e = tid; e < nw * D; e += 2 * D) {
-                const int w = e / D, i = e % D;
-                const int64_t row = (pw + w) * H + h;
-                const float bt = to_f32(beta[row]);
-                sq[w][i] = to_f32(q[row * D + i]);
-                sbk[w][i] = bt * to_f32(k[row * D + i]);
-                se[w][i] = expf(to_f32(g[row * D + i]));
-                sv[w][i] = to_f32(v[row * D + i]);
+#pragma unroll
+            for (int m = 0; m < PER; ++m) {
+                const int e = tid + m * NT;
+                if (e < nw * D) {
+                    sq[e] = rq[m];
+                    sbk[e] = rb[m] * rk[m];
+                    se[e] = expf(rg_[m]);
+                    sv[e] = rv[m];
+                }
             }
+            load_window(pw + kWin);   // in flight while this window is computed
             __syncthreads();
             for (int w = 0; w < nw; ++w) {
-                const float vc = sv[w][c];
-                float acc = 0.f;
+                const float4* r4 = reinterpret_cast<const float4*>(sq + w * D + kTile * rg);
+                const float4 q0 = r4[0], q1 = r4[1];
+                const float4* k4 = reinterpret_cast<const float4*>(sbk + w * D + kTile * rg);
+                const float4 b0 = k4[0], b1 = k4[1];
+                const float4* e4 = reinterpret_cast<const float4*>(se + w * D + kTile * rg);
+                const float4 e0 = e4[0], e1 = e4[1];
+                const float4* v4 = reinterpret_cast<const float4*>(sv + w * D + kTile * cg);
+                const float4 v0 = v4[0], v1 = v4[1];
+                const float qi[kTile] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                const float bi[kTile] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                const float ei[kTile] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+                const float2 vj[kTile / 2] = {make_float2(v0.x, v0.y), make_float2(v0.z, v0.w),
+                                              make_float2(v1.x, v1.y), make_float2(v1.z, v1.w)};
+                float2 acc[kTile / 2];
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int i = half * R + r;
-                    S[r] = fmaf(S[r], se[w][i], sbk[w][i] * vc);
-                    acc = fmaf(sq[w][i], S[r], acc);
+                for (int jp = 0; jp < kTile / 2; ++jp) acc[jp] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < kTile; ++i) {
+                    const float2 e2 = make_float2(ei[i], ei[i]);
+                    const float2 b2 = make_float2(bi[i], bi[i]);
+                    const float2 q2 = make_float2(qi[i], qi[i]);
+#pragma unroll
+                    for (int jp = 0; jp < kTile / 2; ++jp) {
+                        S[i][jp] = rfma2(S[i][jp], e2, rmul2(b2, vj[jp]));   // decay, then add
+                        acc[jp] = rfma2(q2, S[i][jp], acc[jp]);              // read-out after
+                    }
                 }
-                part[half][w][c] = acc;
+                // sum the partial read-outs of the warp's row groups, then one store per column
+#pragma unroll
+                for (int m = NG; m < 32; m <<= 1) {
+#pragma unroll
+                    for (int jp = 0; jp < kTile / 2; ++jp) {
+                        acc[jp].x += __shfl_xor_sync(0xffffffffu, acc[jp].x, m);
+                        acc[jp].y += __shfl_xor_sync(0xffffffffu, acc[jp].y, m);
+                    }
+                }
+                if (lane < NG) {
+                    float4* dst = reinterpret_cast<float4*>(part + (warp * kWin + w) * D + kTile * cg);
+                    dst[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+                    dst[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+                }
             }
             __syncthreads();
-            for (int e = tid; e < nw * D; e += 2 * D) {
+            for (int e = tid; e < nw * D; e += NT) {
                 const int w = e / D, j = e % D;
+                float sum = 0.f;
+#pragma unroll
+                for (int wp = 0; wp < NW; ++wp) sum += part[(wp * kWin + w) * D + j];
                 const int64_t row = (pw + w) * H + h;
-                o[row * D + j] = from_f32<To>(scale * (part[0][w][j] + part[1][w][j]));
+                o[row * D + j] = from_f32<To>(scale * sum);
             }
         }
         if (fin && has_slot) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) fin[slot + int64_t(r) * D] = S[r];
+            for (int i = 0; i < kTile; ++i) {
+                float* dst = fin + slot + int64_t(kTile * rg + i) * D + kTile * cg;
+                *reinterpret_cast<float4*>(dst) = make_float4(S[i][0].x, S[i][0].y, S[i][1].x, S[i][1].y);
+                *reinterpret_cast<float4*>(dst + 4) = make_float4(S[i][2].x, S[i][2].y, S[i][3].x, S[i][3].y);
+            }
         }
     }
 }
@@ -223,14 +320,22 @@ static kda_status_t launch_recurrent_typed(const void* q, const void* k, const v
     const T* gp = static_cast<const T*>(g);
     const T* bp = static_cast<const T*>(beta);
     To* op = static_cast<To*>(o);
-    if (D == 64)
-        recurrent_kernel<T, To, 64><<<blocks, 128, 0, stream>>>(qp, kp, vp, gp, bp, H, scale,
-                                                                seg_start, seg_end, counters, op,
-                                                                init, fin, n_state);
-    else
-        recurrent_kernel<T, To, 128><<<blocks, 256, 0, stream>>>(qp, kp, vp, gp, bp, H, scale,
-                                                                 seg_start, seg_end, counters, op,
-                                                                 init, fin, n_state);
+    if (D == 64) {
+        static const cudaError_t attr = cudaFuncSetAttribute(
+            recurrent_kernel<T, To, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            rec_smem_bytes<64>());
+        if (attr != cudaSuccess) return KDA_ERR_CUDA;
+        recurrent_kernel<T, To, 64><<<blocks, rec_threads<64>(), rec_smem_bytes<64>(), stream>>>(
+            qp, kp, vp, gp, bp, H, scale, seg_start, seg_end, counters, op, init, fin, n_state);
+    } else {
+        static const cudaError_t attr = cudaFuncSetAttribute(
+            recurrent_kernel<T, To, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            rec_smem_bytes<128>());
+        if (attr != cudaSuccess) return KDA_ERR_CUDA;
+        recurrent_kernel<T, To, 128><<<blocks, rec_threads<128>(), rec_smem_bytes<128>(),
+                                       stream>>>(qp, kp, vp, gp, bp, H, scale, seg_start, seg_end,
+                                                 counters, op, init, fin, n_state);
+    }
     return launch_status();
 }
 

@@ -24,6 +24,10 @@
  *     "边界 reset 语义"). The batch is flattened to [1, B*T] ([RFC-0025]
  *     方案 §2), so tensors indexed by token use the flat index p = b*T + t.
  *   - Sizes: B*T < 2^31.
+ *   - Every call can be captured in a CUDA graph: it makes no host round trip,
+ *     allocates nothing and launches only on `stream`. Make one call of each
+ *     entry point (per kernel variant) before capturing, since the first call
+ *     sets kernel attributes.
  */
 #ifndef KDA_H_
 #define KDA_H_

@@ -305,6 +305,21 @@ def run_gb300(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    # per-op times: an eager pass of K steps with CUDA events between the calls
+    for _ in range(args.steps):
+        step(record=True)
+    torch.cuda.synchronize()
+    chunk_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_chunk)
+    seg_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_seg)
+    conv_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_conv) / len(convs)
+    # the timed steps: one step captured in a CUDA graph (the same calls, on the
+    # same buffers) and replayed K times
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
     barrier(ws)
@@ -314,7 +329,7 @@ def run_gb300(args):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
-        step(record=True)
+        graph.replay()
     t1.record(stream)
     torch.cuda.synchronize()
     clocks.mark_stop()
@@ -322,9 +337,6 @@ def run_gb300(args):
     clk = clocks.stop()
     ms_local = t0.elapsed_time(t1) / args.steps
     value, ms = job_throughput(N, ms_local, ws, dev)
-    chunk_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_chunk)
-    seg_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_seg)
-    conv_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_conv) / len(convs)
     real_tokens = int((seg != 0).sum().item())
     if int(status.item()) != 0:
         print(f"warning: device status {int(status.item()):#x}", file=sys.stderr)
@@ -451,6 +463,9 @@ def run_gb300(args):
         "config": {"workload": f"{wl.name} packed: B={wl.B} T={wl.T} H={H} D={wl.d_qk} bf16, "
                                f"max_segs={wl.max_segs}, conv width {wl.k_conv}",
                    "step": "segids->cu_seqlens + 3 masked short convs + chunked KDA fwd",
+                   "timing": ("the step's calls captured once in a CUDA graph, replayed K times "
+                              "between CUDA events; per-op times from an eager pass with events "
+                              "between the calls"),
                    "l2": "inputs larger than L2 (chunk inputs 537 MB, conv inputs 403 MB)",
                    "parallelism": f"replicas x{ws} (rows independent)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",

@@ -177,9 +177,15 @@ kda_status_t kda_chunk_fwd_varlen(const void *q, const void *k, const void *v, c
  * owned by the caller, 16-byte aligned, and must not overlap.
  *
  * The other arguments are those of kda_chunk_fwd_varlen, with the same
- * workspace size. Every dtype runs the token recurrence in fp32 arithmetic
- * (one walk per segment and head); the tensor-core chunked form does not carry
- * per-segment state yet.
+ * workspace size. dtype KDA_BF16 with d_qk == 128 runs the tensor-core
+ * chunked form. It seeds each segment's state at the chunk where the segment
+ * starts and keeps the state carried into the chunk where it ends (in
+ * final_state). A second pass then works chunk by chunk in fp32. It writes
+ * the outputs of each segment's rows in its first chunk, whose read-out of
+ * the initial state the chunked form leaves out, and it forms the final
+ * states. Outputs meet the bf16 bound of kda_chunk_fwd_varlen for either
+ * out_dtype. Other dtypes and widths run the token recurrence in fp32
+ * arithmetic, one walk per segment and head.
  *
  * Returns KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE or
  * KDA_ERR_CUDA. Calls that share a workspace must not overlap in time.

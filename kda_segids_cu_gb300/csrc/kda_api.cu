@@ -17,7 +17,8 @@ kda_status_t launch_recurrent_state(const void* q, const void* k, const void* v,
 kda_status_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* g,
                              const void* beta, const int32_t* seg, int64_t B, int64_t T,
                              int32_t H, int32_t D, float scale, kda_dtype_t out_dtype, void* o,
-                             void* ws, uint32_t* status_dev, cudaStream_t stream);
+                             void* ws, uint32_t* status_dev, const float* init, float* fin,
+                             int64_t n_state, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -107,7 +108,7 @@ kda_status_t kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, c
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == KDA_BF16)
         return kda::launch_chunk_tc(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale,
-                                    out_dtype, o, workspace, status_dev, st);
+                                    out_dtype, o, workspace, status_dev, nullptr, nullptr, 0, st);
     return kda::launch_recurrent(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale, dtype,
                                  out_dtype, o, workspace, st);
 }
@@ -139,9 +140,14 @@ kda_status_t kda_chunk_fwd_varlen_state(const void* q, const void* k, const void
     const size_t need = kda_chunk_fwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
     if (!workspace || workspace_bytes < need || !kda::aligned(workspace, 256))
         return KDA_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == KDA_BF16 && d_qk == 128)   // tensor-core chunked form, then the state pass
+        return kda::launch_chunk_tc(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale,
+                                    out_dtype, o, workspace, status_dev, initial_state,
+                                    final_state, n_state, st);
     return kda::launch_recurrent_state(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale, dtype,
                                        out_dtype, o, workspace, initial_state, final_state,
-                                       n_state, reinterpret_cast<cudaStream_t>(stream));
+                                       n_state, st);
 }
 
 }  // extern "C"

@@ -1,0 +1,51 @@
+// kda_plan.cuh -- the chunk plan that the planner kernels of the bf16 path write into
+// the caller's workspace, read by the chunk kernel and by the per-segment state pass.
+#pragma once
+
+#include "kda_common.cuh"
+
+namespace kda {
+namespace tc {
+
+struct ChunkMeta {
+    unsigned long long start;     // bit i: token i of the chunk starts a segment
+    unsigned long long valid;     // bit i: token i exists and is not padding
+};
+
+struct Plan {                      // device view of the workspace
+    int32_t* counters;             // [0] n_units, [1] next item, [2] n_chunks
+    ChunkMeta* meta;               // [n_chunks]
+    int32_t* first_cut;            // [n_chunks] first start-or-padding row, 64 if none
+    int32_t* block_cut;            // [n_blocks]
+    int32_t* cut_list;             // [n_chunks]
+    int4* units;                   // [n_chunks] (c0, c1, row_lo, row_hi)
+    int32_t* order;                // [n_chunks] unit indices, longest first
+    int32_t* rank_base;            // [n_chunks] segment starts before the chunk (state calls only)
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline size_t plan_bytes(int64_t n_chunks) {
+    size_t b = align256(64 * sizeof(int32_t));
+    b += align256(n_chunks * sizeof(ChunkMeta));
+    b += align256(n_chunks * sizeof(int32_t)) * 5;   // first_cut, block_cut, cut_list, order, rank_base
+    b += align256(n_chunks * sizeof(int4));
+    return b;
+}
+
+__host__ __device__ inline Plan plan_view(void* ws, int64_t n_chunks) {
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    Plan pl;
+    pl.counters = reinterpret_cast<int32_t*>(p);      p += align256(64 * sizeof(int32_t));
+    pl.meta = reinterpret_cast<ChunkMeta*>(p);        p += align256(n_chunks * sizeof(ChunkMeta));
+    pl.first_cut = reinterpret_cast<int32_t*>(p);     p += align256(n_chunks * sizeof(int32_t));
+    pl.block_cut = reinterpret_cast<int32_t*>(p);     p += align256(n_chunks * sizeof(int32_t));
+    pl.cut_list = reinterpret_cast<int32_t*>(p);      p += align256(n_chunks * sizeof(int32_t));
+    pl.order = reinterpret_cast<int32_t*>(p);         p += align256(n_chunks * sizeof(int32_t));
+    pl.rank_base = reinterpret_cast<int32_t*>(p);     p += align256(n_chunks * sizeof(int32_t));
+    pl.units = reinterpret_cast<int4*>(p);
+    return pl;
+}
+
+}  // namespace tc
+}  // namespace kda

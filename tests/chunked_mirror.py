@@ -90,3 +90,131 @@ def chunked_forward(q, k, v, g, beta, seg, B, T, scale=1.0, round_bf16=False,
             S = S_new
             o[lo_p:hi_p, h] = scale * O[:n]
     return torch.from_numpy(o)
+
+
+def chunked_forward_state(q, k, v, g, beta, seg, B, T, init=None, n_state=0, want_final=False,
+                          scale=1.0):
+    """The per-segment state split of the bf16 path, in float64: the chunk walk above
+    with the state seeded at the chunk where a segment starts (its initial state decayed
+    to the chunk's end) and the state carried into the chunk where a segment ends kept
+    aside; then the per-chunk pass that writes the rows of each segment in its first
+    chunk whole and forms the final states. Segment r (flattened order) has slot r if
+    r < n_state. Returns (o [N, H, Dv], final [n_state, H, Dk, Dv] or None)."""
+    f = (lambda t: t.detach().to(torch.float64).numpy()) if isinstance(q, torch.Tensor) else np.asarray
+    q, k, v, g, beta = (f(t) for t in (q, k, v, g, beta))
+    S0 = None if init is None else f(init)
+    N, H, Dk = q.shape
+    Dv = v.shape[-1]
+    ids = np.ones(N, dtype=np.int64) if seg is None else \
+        (seg.numpy() if isinstance(seg, torch.Tensor) else np.asarray(seg)).reshape(-1)
+    p = np.arange(N)
+    valid_all = ids != 0
+    prev = np.concatenate([[0], ids[:-1]])
+    start_all = valid_all & ((p % T == 0) | (ids != prev))
+    n_chunks = (N + C - 1) // C
+
+    def chunk_masks(c):
+        lo_p, hi_p = c * C, min((c + 1) * C, N)
+        valid = np.zeros(C, bool)
+        start = np.zeros(C, bool)
+        valid[: hi_p - lo_p] = valid_all[lo_p:hi_p]
+        start[: hi_p - lo_p] = start_all[lo_p:hi_p]
+        return valid, start
+
+    first_cut = np.zeros(n_chunks, int)
+    rank_base = np.zeros(n_chunks, int)
+    run = 0
+    for c in range(n_chunks):
+        valid, start = chunk_masks(c)
+        cut = np.nonzero(start | ~valid)[0]
+        first_cut[c] = cut[0] if len(cut) else C
+        rank_base[c] = run
+        run += int(start.sum())
+    fin = np.zeros((n_state, H, Dk, Dv)) if want_final else None
+    o = np.zeros((N, H, Dv))
+
+    def rows_of(c, h, arr):
+        lo_p, hi_p = c * C, min((c + 1) * C, N)
+        out = np.zeros((C,) + arr.shape[2:])
+        out[: hi_p - lo_p] = arr[lo_p:hi_p, h]
+        return out
+
+    for h in range(H):
+        # ---- chunk walk (the tensor-core kernel): zero start, seeds, exports ----
+        S = np.zeros((Dk, Dv))
+        for c in range(n_chunks):
+            lo_p, hi_p = c * C, min((c + 1) * C, N)
+            n = hi_p - lo_p
+            valid, start = chunk_masks(c)
+            fc = first_cut[c]
+            starts = np.nonzero(start)[0]
+            last_start = starts[-1] if len(starts) else 0
+            tail_live = valid[C - 1]
+            next_cut = c + 1 >= n_chunks or first_cut[c + 1] == 0
+            read_state = fc > 0 and c > 0
+            carry = fc == C and c > 0
+            gg = np.where(valid[:, None], rows_of(c, h, g), 0.0)
+            G = np.cumsum(gg, axis=0)                      # G_i, inclusive
+            qq, kk, vv, bb = rows_of(c, h, q), rows_of(c, h, k), rows_of(c, h, v), rows_of(c, h, beta)
+            rows = np.arange(C)
+            lo = np.array([(np.nonzero(start[: i + 1])[0][-1] if start[: i + 1].any() else 0)
+                           for i in range(C)])
+            if want_final and read_state and (fc < C or next_cut) and rank_base[c] - 1 < n_state:
+                fin[rank_base[c] - 1, h] = S                # exported S_in
+            O = np.zeros((C, Dv))
+            for i in range(C):
+                if not valid[i]:
+                    continue
+                for j in range(lo[i], i + 1):
+                    O[i] += (qq[i] * np.exp(G[i] - G[j])) @ kk[j] * bb[j] * vv[j]
+                if read_state and i < fc:
+                    O[i] += (qq[i] * np.exp(G[i])) @ S
+            Snew = np.zeros((Dk, Dv))
+            if tail_live:
+                for j in range(last_start, C):
+                    Snew += np.outer(kk[j] * bb[j] * np.exp(G[-1] - G[j]), vv[j])
+            if carry:
+                Snew += np.exp(G[-1])[:, None] * S
+            rl = rank_base[c] + len(starts) - 1
+            if S0 is not None and tail_live and len(starts) and rl < n_state:
+                base = G[last_start - 1] if last_start > 0 else np.zeros(Dk)
+                Snew += np.exp(G[-1] - base)[:, None] * S0[rl, h]
+            S = Snew
+            o[lo_p:hi_p, h] = scale * O[:n]
+        # ---- the state pass: per chunk, local work ----
+        for c in range(n_chunks):
+            lo_p, hi_p = c * C, min((c + 1) * C, N)
+            valid, start = chunk_masks(c)
+            fc = first_cut[c]
+            next_cut = c + 1 >= n_chunks or first_cut[c + 1] == 0
+            rb = rank_base[c]
+            cut = start | ~valid
+            gg = np.where(valid[:, None], rows_of(c, h, g), 0.0)
+            G = np.cumsum(gg, axis=0)
+            Gm = lambda i: G[i] if i >= 0 else np.zeros(Dk)   # noqa: E731
+            qq, kk, vv, bb = rows_of(c, h, q), rows_of(c, h, k), rows_of(c, h, v), rows_of(c, h, beta)
+
+            def final(a, e, base):
+                Sx = np.zeros((Dk, Dv)) if base is None else np.exp(G[e] - Gm(a - 1))[:, None] * base
+                for j in range(a, e + 1):
+                    Sx = Sx + np.outer(bb[j] * kk[j] * np.exp(G[e] - G[j]), vv[j])
+                return Sx
+
+            if want_final and fc > 0 and (fc < C or next_cut) and rb - 1 < n_state:
+                fin[rb - 1, h] = final(0, min(fc, C) - 1, fin[rb - 1, h])
+            for idx, r in enumerate(np.nonzero(start)[0]):
+                rank = rb + idx
+                if rank >= n_state:
+                    break
+                after = np.nonzero(cut[r + 1:])[0]
+                end = r + 1 + after[0] if len(after) else C
+                ends_here = len(after) > 0 or next_cut
+                if S0 is not None:
+                    for t in range(r, end):
+                        acc = (qq[t] * np.exp(G[t] - Gm(r - 1))) @ S0[rank, h]
+                        for j in range(r, t + 1):
+                            acc = acc + (qq[t] * np.exp(G[t] - G[j])) @ kk[j] * bb[j] * vv[j]
+                        o[lo_p + t, h] = scale * acc
+                if want_final and ends_here:
+                    fin[rank, h] = final(r, end - 1, None if S0 is None else S0[rank, h])
+    return torch.from_numpy(o), (None if fin is None else torch.from_numpy(fin))

@@ -2,9 +2,11 @@
 
 Segment r (flattened token order) starts from initial_state[r] and returns its
 state after its last token in final[r]. Outputs are held to the bounds of
-kda_chunk_fwd_varlen (this entry runs the fp32 token recurrence for every dtype,
-so the fp32 bound 1e-4 RMS applies to fp32 outputs of either input dtype); final
-states to max|S - S_ref| <= 1e-4 RMS(S_ref) per (segment, head).
+kda_chunk_fwd_varlen for the input dtype. bf16 inputs with 128-wide heads run the
+tensor-core chunked form plus the state pass, so they get the bf16 bound for
+either output dtype. The other cases run the fp32 token recurrence, so their fp32
+outputs get the fp32 bound of 1e-4 RMS. Final states are held to
+max|S - S_ref| <= 1e-4 RMS(S_ref) per (segment, head).
 """
 import numpy as np
 import pytest
@@ -28,6 +30,24 @@ def _n_segments(seg, B):
     return int(start.sum())
 
 
+def _first_chunk_rows(seg):
+    """Mask of the flattened tokens that lie in their segment's first 64-token chunk."""
+    s = seg.reshape(-1).numpy()
+    B, T = seg.shape
+    out = np.zeros(s.shape[0], bool)
+    p = 0
+    while p < s.shape[0]:
+        if s[p] == 0:
+            p += 1
+            continue
+        e = p + 1
+        while e < s.shape[0] and s[e] == s[p] and e % T != 0:
+            e += 1
+        out[p:min(e, (p // 64 + 1) * 64)] = True
+        p = e
+    return torch.from_numpy(out).cuda()
+
+
 def _check_states(fin, ref, label):
     fin = fin.double().cpu()
     for r in range(ref.shape[0]):
@@ -35,6 +55,11 @@ def _check_states(fin, ref, label):
             rms = ref[r, h].pow(2).mean().sqrt().item()
             err = (fin[r, h] - ref[r, h]).abs().max().item()
             assert err <= 1e-4 * rms + 1e-30, f"{label}: state [{r},{h}] err {err:.3e} rms {rms:.3e}"
+
+
+def _o_bound(dtype, D):
+    """Input dtype whose bound an fp32 output of the state call meets."""
+    return dtype if (dtype == torch.bfloat16 and D == 128) else torch.float32
 
 
 def _run(inp, B, T, init, n_state, out_dtype=None, seg="inputs"):
@@ -59,7 +84,7 @@ def test_states_match_oracle(name):
                                         wl.B, wl.T, initial_state=init, n_state=n,
                                         want_final=True)
     o32, fin = _run(inp, wl.B, wl.T, init, n, out_dtype=torch.float32)
-    check_kda_output(o32, ref, inp.segment_ids, torch.float32, label=name + "/f32 out")
+    check_kda_output(o32, ref, inp.segment_ids, _o_bound(wl.dtype, D), label=name + "/f32 out")
     _check_states(fin, ref_fin, name)
     o, fin2 = _run(inp, wl.B, wl.T, init, n)
     check_kda_output(o, ref, inp.segment_ids, wl.dtype, label=name)
@@ -69,8 +94,10 @@ def test_states_match_oracle(name):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("D", [64, 128])
 def test_partial_slots_and_zero_state(dtype, D):
-    """Segments past n_state start from zero and are not written; a zero initial
-    state gives the plain entry point's result (fp32: the same kernel, bit for bit)."""
+    """Segments past n_state start from zero and are not written. A zero initial state
+    gives the plain entry point's result bit for bit: the same kernels, and on the
+    tensor-core path a seed of zeros adds nothing. The exception is the rows of each
+    segment in the chunk where it starts, which the state pass rewrites in fp32."""
     B, T, H = 2, 150, 2
     inp = _small_random(B, T, H, D, dtype, seed=D, max_len=40, pad_prob=0.1)
     seg = inp.segment_ids
@@ -80,20 +107,22 @@ def test_partial_slots_and_zero_state(dtype, D):
     ref, ref_fin = oracle.kda_fwd_state(inp.q, inp.k, inp.v, inp.g, inp.beta, seg, B, T,
                                         initial_state=init, n_state=k, want_final=True)
     o32, fin = _run(inp, B, T, init, k, out_dtype=torch.float32)
-    check_kda_output(o32, ref, seg, torch.float32, label=f"partial D={D}")
+    check_kda_output(o32, ref, seg, _o_bound(dtype, D), label=f"partial D={D}")
     _check_states(fin, ref_fin, f"partial D={D}")
     zero = torch.zeros(n, H, D, D)
     oz, _ = _run(inp, B, T, zero, n, out_dtype=torch.float32)
     plain = kda.kda_chunk_fwd_varlen(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), inp.g.cuda(),
                                      inp.beta.cuda(), seg.cuda(), B=B, T=T,
                                      out_dtype=torch.float32)
-    if dtype == torch.float32:
-        assert torch.equal(oz, plain)
-    else:
+    if dtype == torch.bfloat16 and D == 128:
+        keep = ~_first_chunk_rows(seg)
+        assert torch.equal(oz[keep], plain[keep])
         check_kda_output(oz, oracle.kda_fwd(inp.q, inp.k, inp.v, inp.g, inp.beta, seg, B, T),
-                         seg, torch.float32, label=f"zero state D={D}")
-        check_kda_output(plain, oracle.kda_fwd(inp.q, inp.k, inp.v, inp.g, inp.beta, seg, B, T),
-                         seg, dtype, label=f"plain D={D}")
+                         seg, dtype, label=f"zero state D={D}")
+    else:
+        assert torch.equal(oz, plain)
+    check_kda_output(plain, oracle.kda_fwd(inp.q, inp.k, inp.v, inp.g, inp.beta, seg, B, T),
+                     seg, dtype, label=f"plain D={D}")
 
 
 def test_chaining_on_gpu():
@@ -122,3 +151,63 @@ def test_segment_ids_none_ranks_rows():
     o1, f1 = _run(inp, B, T, init, B, seg=ones)
     on, fn = _run(inp, B, T, init, B, seg=None)
     assert torch.equal(o1, on) and torch.equal(f1, fn)
+
+
+def _layout_inputs(kind, seed):
+    """bf16, 128-wide heads: layouts that exercise every case of the state split."""
+    if kind == "long":          # documents across many chunks, one ending on a chunk edge
+        B, T = 1, 1100
+        ids = [1] * 600 + [2] * 104 + [3] * 396
+    elif kind == "edges":       # length-1 documents on both sides of chunk edges
+        ids = [1] * 63 + [2] + [3] + [4] * 62 + [5] + [6] * 129 + [7] * 64
+        B, T = 1, len(ids)
+    elif kind == "aligned":     # documents on chunk edges, then padding
+        B, T = 2, 256
+        ids = [1] * 64 + [2] * 128 + [0] * 64 + [3] * 192 + [4] * 64
+    else:
+        ids = None
+    if ids is not None:
+        inp = _small_random(B, T, 3, 128, torch.bfloat16, seed=seed)
+        inp.segment_ids = torch.tensor(ids, dtype=torch.int32).reshape(B, T)
+        return inp, B, T
+    B, T = 2, 300               # many short documents per chunk, padding, ragged T
+    return _small_random(B, T, 3, 128, torch.bfloat16, seed=seed, max_len=20, pad_prob=0.1), B, T
+
+
+@pytest.mark.parametrize("kind", ["long", "edges", "aligned", "short"])
+@pytest.mark.parametrize("mode", ["init+final", "init", "final", "half-slots"])
+def test_tensor_core_state_layouts(kind, mode):
+    inp, B, T = _layout_inputs(kind, seed=len(kind) + 3 * len(mode))
+    n = _n_segments(inp.segment_ids, B)
+    H, D = 3, 128
+    n_state = max(1, n // 2) if mode == "half-slots" else n
+    gen = torch.Generator().manual_seed(n_state)
+    init = torch.randn(n_state, H, D, D, generator=gen) * 0.5 if mode != "final" else None
+    want = mode != "init"
+    ref, ref_fin = oracle.kda_fwd_state(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.segment_ids,
+                                        B, T, initial_state=init, n_state=n_state,
+                                        want_final=want)
+    o, fin = kda.kda_chunk_fwd_varlen_state(
+        inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), inp.g.cuda(), inp.beta.cuda(),
+        inp.segment_ids.cuda(), B=B, T=T, initial_state=None if init is None else init.cuda(),
+        output_final_state=want, n_state=n_state)
+    torch.cuda.synchronize()
+    check_kda_output(o, ref, inp.segment_ids, torch.bfloat16, label=f"{kind}/{mode}")
+    if want:
+        _check_states(fin, ref_fin, f"{kind}/{mode}")
+
+
+def test_tensor_core_chaining():
+    """bf16, 128-wide heads: a document cut in two (mid-chunk), with part A's final state
+    handed to part B, gives the uncut document's outputs and final state."""
+    T, H, D, m = 700, 2, 128, 333
+    inp = _small_random(1, T, H, D, torch.bfloat16, seed=9)
+    whole = torch.ones(1, T, dtype=torch.int32)
+    cut = torch.tensor([[1] * m + [2] * (T - m)], dtype=torch.int32)
+    init = torch.randn(1, H, D, D, generator=torch.Generator().manual_seed(2)) * 0.3
+    ref, ref_fin = oracle.kda_fwd_state(inp.q, inp.k, inp.v, inp.g, inp.beta, whole, 1, T,
+                                        initial_state=init, n_state=1, want_final=True)
+    _, f_a = _run(inp, 1, T, torch.cat([init, init]), 2, seg=cut)
+    o_c, f_c = _run(inp, 1, T, torch.cat([init, f_a[:1].cpu()]), 2, seg=cut)
+    check_kda_output(o_c, ref, whole, torch.bfloat16, label="chained")
+    _check_states(f_c[1:], ref_fin, "chained")

@@ -13,7 +13,7 @@ struct ChunkMeta {
 };
 
 struct Plan {                      // device view of the workspace
-    int32_t* counters;             // [0] n_units, [1] next item, [2] n_chunks
+    int32_t* counters;             // [0] n_units, [1] next item, [2] n_chunks, [3] n_active
     ChunkMeta* meta;               // [n_chunks]
     int32_t* first_cut;            // [n_chunks] first start-or-padding row, 64 if none
     int32_t* block_cut;            // [n_blocks]
@@ -21,6 +21,8 @@ struct Plan {                      // device view of the workspace
     int4* units;                   // [n_chunks] (c0, c1, row_lo, row_hi)
     int32_t* order;                // [n_chunks] unit indices, longest first
     int32_t* rank_base;            // [n_chunks] segment starts before the chunk (state calls only)
+    int32_t* active;               // [n_chunks] chunks holding a start or a carried segment's end
+                                   // (state calls only), in order
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -28,7 +30,8 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 __host__ __device__ inline size_t plan_bytes(int64_t n_chunks) {
     size_t b = align256(64 * sizeof(int32_t));
     b += align256(n_chunks * sizeof(ChunkMeta));
-    b += align256(n_chunks * sizeof(int32_t)) * 5;   // first_cut, block_cut, cut_list, order, rank_base
+    b += align256(n_chunks * sizeof(int32_t)) * 6;   // first_cut, block_cut, cut_list, order,
+                                                     // rank_base, active
     b += align256(n_chunks * sizeof(int4));
     return b;
 }
@@ -43,6 +46,7 @@ __host__ __device__ inline Plan plan_view(void* ws, int64_t n_chunks) {
     pl.cut_list = reinterpret_cast<int32_t*>(p);      p += align256(n_chunks * sizeof(int32_t));
     pl.order = reinterpret_cast<int32_t*>(p);         p += align256(n_chunks * sizeof(int32_t));
     pl.rank_base = reinterpret_cast<int32_t*>(p);     p += align256(n_chunks * sizeof(int32_t));
+    pl.active = reinterpret_cast<int32_t*>(p);        p += align256(n_chunks * sizeof(int32_t));
     pl.units = reinterpret_cast<int4*>(p);
     return pl;
 }

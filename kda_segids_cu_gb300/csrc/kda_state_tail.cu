@@ -21,8 +21,8 @@
 //     the final state
 //         S_e = exp(G_e - G_{a-1}) * S_a + sum_{j=a..e} (beta_j k_j * exp(G_e - G_j)) v_j^T
 //     where the products with exp(...) scale the key rows.
-// One CTA takes one (chunk, head) at a time and passes over those with nothing to do.
-// fp32 arithmetic with exact exponentials (expf).
+// The planner lists the chunks holding a start or the end of a carried segment; one CTA
+// takes one (listed chunk, head) at a time. fp32 arithmetic with exact exponentials (expf).
 #include "kda_common.cuh"
 #include "kda_plan.cuh"
 
@@ -32,10 +32,12 @@ namespace {
 
 constexpr int kTD = 128;                  // head width of the bf16 path
 constexpr int kTR = kChunk;               // rows per chunk
-constexpr int kTailThreads = 256;
-// shared memory (bytes): q, k, v as stored (bf16 [64][128], row-major), the cumulative
-// log-decay G [64][128] and work arrays W [128][64] or [64][128] and X [128][64] (fp32; W
-// holds g as bf16 while G is formed), a score tile A [64][64] and beta [64] (fp32)
+constexpr int kTailThreads = 512;
+constexpr int kTailWarps = kTailThreads / 32;
+// shared memory (bytes): q, k, v as stored (bf16 [64][128], row-major); the cumulative
+// log-decay G [64][128]; work arrays W ([128][64] or [64][128]) and X ([128][64], or 64 rows
+// of an initial state), fp32 (W holds g as bf16 while G is formed); a score tile A [64][64],
+// beta [64] and G's per-quarter sums [4][128], fp32
 constexpr uint32_t kSq = 0;
 constexpr uint32_t kSk = kSq + kTR * kTD * 2;
 constexpr uint32_t kSv = kSk + kTR * kTD * 2;
@@ -44,7 +46,8 @@ constexpr uint32_t kSW = kSG + kTR * kTD * 4;
 constexpr uint32_t kSX = kSW + kTR * kTD * 4;
 constexpr uint32_t kSA = kSX + kTR * kTD * 4;
 constexpr uint32_t kSB = kSA + kTR * kTR * 4;
-constexpr uint32_t kTailSmem = kSB + kTR * 4;   // 164,096 B: one CTA per SM
+constexpr uint32_t kSQ = kSB + kTR * 4;
+constexpr uint32_t kTailSmem = kSQ + 4 * kTD * 4;   // 166,144 B: one CTA per SM
 
 __device__ __forceinline__ float2 pfma(float2 a, float2 b, float2 c) {
     float2 d;
@@ -55,14 +58,10 @@ __device__ __forceinline__ float2 pfma(float2 a, float2 b, float2 c) {
     return d;
 }
 
-// 8 bf16 (one 16-byte word) -> 8 floats; exact (bf16 is the top half of an fp32 word)
-__device__ __forceinline__ void unpack8(uint4 w, float* x) {
-    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        x[2 * i] = __uint_as_float(a[i] << 16);
-        x[2 * i + 1] = __uint_as_float(a[i] & 0xffff0000u);
-    }
+// 4 bf16 (one 8-byte word) -> 2 float pairs; exact (bf16 is the top half of an fp32 word)
+__device__ __forceinline__ void unpack4(uint2 w, float2* x) {
+    x[0] = make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+    x[1] = make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -70,16 +69,22 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// dst[0..7] = scale * acc (one 16- or 32-byte group of an output row), rounded once
+// dst[0..3] = scale * acc (4 channels of an output row), rounded once
 __device__ __forceinline__ void store_out(__nv_bfloat16* dst, const float2* acc, float scale) {
-    *reinterpret_cast<uint4*>(dst) =
-        make_uint4(pack2(scale * acc[0].x, scale * acc[0].y), pack2(scale * acc[1].x, scale * acc[1].y),
-                   pack2(scale * acc[2].x, scale * acc[2].y), pack2(scale * acc[3].x, scale * acc[3].y));
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(pack2(scale * acc[0].x, scale * acc[0].y), pack2(scale * acc[1].x, scale * acc[1].y));
 }
 __device__ __forceinline__ void store_out(float* dst, const float2* acc, float scale) {
-    float4* p = reinterpret_cast<float4*>(dst);
-    p[0] = make_float4(scale * acc[0].x, scale * acc[0].y, scale * acc[1].x, scale * acc[1].y);
-    p[1] = make_float4(scale * acc[2].x, scale * acc[2].y, scale * acc[3].x, scale * acc[3].y);
+    *reinterpret_cast<float4*>(dst) =
+        make_float4(scale * acc[0].x, scale * acc[0].y, scale * acc[1].x, scale * acc[1].y);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 struct Tile {                              // shared-memory views of the current (chunk, head)
@@ -91,11 +96,12 @@ struct Tile {                              // shared-memory views of the current
     float* X;
     float* A;
     const float* beta;
+    uint32_t x_addr;                       // shared-state-space address of X
 };
 
 // Final state of rows a..e (one segment): out = exp(G_e - G_{a-1}) * base + sum_j Kf_j v_j^T,
 // Kf_j = beta_j k_j * exp(G_e - G_j). base may be null (zero) or equal to out (in place:
-// each thread reads its own 8 x 8 block before writing it).
+// each thread reads its own 8 x 4 block before writing it).
 __device__ void final_state(const Tile& t, int a, int e, const float* base, float* out) {
     const int tid = threadIdx.x;
     const float* Ge = t.G + e * kTD;
@@ -105,22 +111,18 @@ __device__ void final_state(const Tile& t, int a, int e, const float* base, floa
                            expf(Ge[c] - t.G[j * kTD + c]);
     }
     __syncthreads();
-    const int rg = tid >> 4, cg = tid & 15;        // key rows 8 rg .., value columns 8 cg ..
-    float2 acc[8][4];
+    const int rg = tid >> 5, cg = tid & 31;        // key rows 8 rg .., value columns 4 cg ..
+    float2 acc[8][2];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int c = 8 * rg + i;
         const float dec = expf(Ge[c] - (a > 0 ? t.G[(a - 1) * kTD + c] : 0.f));
         if (base) {
-            const float4* b4 = reinterpret_cast<const float4*>(base + c * kTD + 8 * cg);
-            const float4 x = b4[0], y = b4[1];
+            const float4 x = *reinterpret_cast<const float4*>(base + c * kTD + 4 * cg);
             acc[i][0] = make_float2(dec * x.x, dec * x.y);
             acc[i][1] = make_float2(dec * x.z, dec * x.w);
-            acc[i][2] = make_float2(dec * y.x, dec * y.y);
-            acc[i][3] = make_float2(dec * y.z, dec * y.w);
         } else {
-#pragma unroll
-            for (int jp = 0; jp < 4; ++jp) acc[i][jp] = make_float2(0.f, 0.f);
+            acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
         }
     }
 #pragma unroll 2
@@ -128,40 +130,38 @@ __device__ void final_state(const Tile& t, int a, int e, const float* base, floa
         const float4* w4 = reinterpret_cast<const float4*>(t.W + j * kTD + 8 * rg);
         const float4 w0 = w4[0], w1 = w4[1];
         const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        float vv[8];
-        unpack8(*reinterpret_cast<const uint4*>(t.v + j * kTD + 8 * cg), vv);
+        float2 vv[2];
+        unpack4(*reinterpret_cast<const uint2*>(t.v + j * kTD + 4 * cg), vv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float2 wi = make_float2(w[i], w[i]);
-#pragma unroll
-            for (int jp = 0; jp < 4; ++jp)
-                acc[i][jp] = pfma(wi, make_float2(vv[2 * jp], vv[2 * jp + 1]), acc[i][jp]);
+            acc[i][0] = pfma(wi, vv[0], acc[i][0]);
+            acc[i][1] = pfma(wi, vv[1], acc[i][1]);
         }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        float4* d4 = reinterpret_cast<float4*>(out + (8 * rg + i) * kTD + 8 * cg);
-        d4[0] = make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
-        d4[1] = make_float4(acc[i][2].x, acc[i][2].y, acc[i][3].x, acc[i][3].y);
-    }
+    for (int i = 0; i < 8; ++i)
+        *reinterpret_cast<float4*>(out + (8 * rg + i) * kTD + 4 * cg) =
+            make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
     __syncthreads();                              // W is free again
 }
 
 // Outputs of rows r..end-1, the rows of a segment (with initial state S0) in the chunk
 // where it starts: o_t = scale (Qd_t^T S0 + sum_{j=r..t} (Qd_t . Kd_j) v_j). Qd and Kd are
 // kept transposed (W, X: [key channel][row]) and so is the score tile (A: [j][t]), so that
-// the loops below read 16-byte groups without bank conflicts.
+// the loops below read 8- and 16-byte groups without bank conflicts; S0 then passes through
+// X, 64 key rows at a time.
 template <typename To>
 __device__ void head_output(const Tile& t, int r, int end, const float* __restrict__ S0,
                             To* o, int64_t p0, int32_t H, int h, float scale) {
     const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
     {
         // transposing writes: a warp takes 32 rows x 32 key channels along a diagonal
         // (lane l: row 32 rt + l, channel 32 ct + (l + d) % 32), so that both the row-major
         // reads and the column-major writes fall in 32 different banks
-        const int lane = tid & 31, warp = tid >> 5;
         const int n_units = ((end - r + 31) / 32) * (kTD / 32) * 32;
-        for (int wu = warp; wu < n_units; wu += kTailThreads / 32) {
+        for (int wu = warp; wu < n_units; wu += kTailWarps) {
             const int rt = wu / (kTD / 32 * 32), ct = (wu / 32) % (kTD / 32), d = wu % 32;
             const int i = r + rt * 32 + lane;
             const int c = ct * 32 + ((lane + d) & 31);
@@ -175,16 +175,16 @@ __device__ void head_output(const Tile& t, int r, int end, const float* __restri
     }
     __syncthreads();
     {                                             // A[j][t] = Qd_t . Kd_j for r <= j <= t < end
-        const int ta = tid >> 4, jb = tid & 15;   // rows t 4 ta .. +3, columns j 4 jb .. +3
-        float acc[4][4] = {};
-        if (4 * ta + 3 >= r && 4 * ta < end && 4 * jb < end && 4 * jb <= 4 * ta + 3) {
+        const int ta = tid >> 4, jb = tid & 15;   // rows t 2 ta, 2 ta + 1; columns j 4 jb .. +3
+        float acc[2][4] = {};
+        if (2 * ta + 1 >= r && 2 * ta < end && 4 * jb < end && 4 * jb <= 2 * ta + 1) {
 #pragma unroll 4
             for (int c = 0; c < kTD; ++c) {
-                const float4 w = *reinterpret_cast<const float4*>(t.W + c * kTR + 4 * ta);
+                const float2 w = *reinterpret_cast<const float2*>(t.W + c * kTR + 2 * ta);
                 const float4 x = *reinterpret_cast<const float4*>(t.X + c * kTR + 4 * jb);
-                const float wv[4] = {w.x, w.y, w.z, w.w}, xv[4] = {x.x, x.y, x.z, x.w};
+                const float wv[2] = {w.x, w.y}, xv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < 2; ++i)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(wv[i], xv[j], acc[i][j]);
             }
@@ -192,62 +192,70 @@ __device__ void head_output(const Tile& t, int r, int end, const float* __restri
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int jj = 4 * jb + j;
-            float out[4];
+            float out[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int ti = 4 * ta + i;
+            for (int i = 0; i < 2; ++i) {
+                const int ti = 2 * ta + i;
                 out[i] = (jj >= r && jj <= ti && ti < end) ? acc[i][j] : 0.f;
             }
-            *reinterpret_cast<float4*>(t.A + jj * kTR + 4 * ta) = make_float4(out[0], out[1], out[2], out[3]);
+            *reinterpret_cast<float2*>(t.A + jj * kTR + 2 * ta) = make_float2(out[0], out[1]);
         }
     }
-    __syncthreads();
-    const int tr = tid >> 4, cg = tid & 15;        // rows 4 tr .. +3, value columns 8 cg ..
+    __syncthreads();                              // X (Kd) is free: S0 goes through it
+    const int tr = tid >> 5, cg = tid & 31;        // rows 4 tr .. +3, value columns 4 cg ..
     const int i0 = 4 * tr;
-    if (i0 + 3 >= r && i0 < end) {
-        float2 acc[4][4];
+    const bool mine = i0 + 3 >= r && i0 < end;
+    float2 acc[4][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {        // Qd^T S0, key rows 64 half .. +63
 #pragma unroll
-            for (int jp = 0; jp < 4; ++jp) acc[i][jp] = make_float2(0.f, 0.f);
+        for (int mm = 0; mm < kTR * kTD / 4 / kTailThreads; ++mm) {
+            const int idx = tid + mm * kTailThreads;          // 16-byte group of the 32 KB block
+            cp_async16(t.x_addr + idx * 16, S0 + (64 * half) * kTD + idx * 4, 16);
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        if (mine) {
 #pragma unroll 4
-        for (int c = 0; c < kTD; ++c) {           // Qd^T S0
-            const float4 s0 = __ldg(reinterpret_cast<const float4*>(S0 + c * kTD + 8 * cg));
-            const float4 s1 = __ldg(reinterpret_cast<const float4*>(S0 + c * kTD + 8 * cg + 4));
-            const float2 sv[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w),
-                                  make_float2(s1.x, s1.y), make_float2(s1.z, s1.w)};
-            const float4 w = *reinterpret_cast<const float4*>(t.W + c * kTR + i0);
-            const float wv[4] = {w.x, w.y, w.z, w.w};
+            for (int cc = 0; cc < 64; ++cc) {
+                const float4 w = *reinterpret_cast<const float4*>(t.W + (64 * half + cc) * kTR + i0);
+                const float4 sv4 = *reinterpret_cast<const float4*>(t.X + cc * kTD + 4 * cg);
+                const float2 sv[2] = {make_float2(sv4.x, sv4.y), make_float2(sv4.z, sv4.w)};
+                const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 w2 = make_float2(wv[i], wv[i]);
-#pragma unroll
-                for (int jp = 0; jp < 4; ++jp) acc[i][jp] = pfma(w2, sv[jp], acc[i][jp]);
+                for (int i = 0; i < 4; ++i) {
+                    const float2 w2 = make_float2(wv[i], wv[i]);
+                    acc[i][0] = pfma(w2, sv[0], acc[i][0]);
+                    acc[i][1] = pfma(w2, sv[1], acc[i][1]);
+                }
             }
         }
+        __syncthreads();                          // X is read before it is refilled
+    }
+    if (mine) {
         const int j_hi = (i0 + 4 < end) ? i0 + 4 : end;
         for (int j = r; j < j_hi; ++j) {          // + A V (A is zero outside the segment)
             const float4 a = *reinterpret_cast<const float4*>(t.A + j * kTR + i0);
             const float av[4] = {a.x, a.y, a.z, a.w};
-            float vv[8];
-            unpack8(*reinterpret_cast<const uint4*>(t.v + j * kTD + 8 * cg), vv);
+            float2 vv[2];
+            unpack4(*reinterpret_cast<const uint2*>(t.v + j * kTD + 4 * cg), vv);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float2 a2 = make_float2(av[i], av[i]);
-#pragma unroll
-                for (int jp = 0; jp < 4; ++jp)
-                    acc[i][jp] = pfma(a2, make_float2(vv[2 * jp], vv[2 * jp + 1]), acc[i][jp]);
+                acc[i][0] = pfma(a2, vv[0], acc[i][0]);
+                acc[i][1] = pfma(a2, vv[1], acc[i][1]);
             }
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int row = i0 + i;
             if (row < r || row >= end) continue;
-            To* dst = o + ((p0 + row) * H + h) * kTD + 8 * cg;
-            store_out(dst, acc[i], scale);
+            store_out(o + ((p0 + row) * H + h) * kTD + 4 * cg, acc[i], scale);
         }
     }
-    __syncthreads();                              // W, X and A are free again
+    __syncthreads();                              // W and A are free again
 }
 
 template <typename To>
@@ -258,6 +266,7 @@ state_tail_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                   void* ws, const float* __restrict__ init, float* fin, int64_t n_state,
                   To* o) {
     extern __shared__ __align__(16) uint8_t sm[];
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
     Tile t;
     t.q = reinterpret_cast<const __nv_bfloat16*>(sm + kSq);
     t.k = reinterpret_cast<const __nv_bfloat16*>(sm + kSk);
@@ -267,13 +276,15 @@ state_tail_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     t.X = reinterpret_cast<float*>(sm + kSX);
     t.A = reinterpret_cast<float*>(sm + kSA);
     t.beta = reinterpret_cast<const float*>(sm + kSB);
+    t.x_addr = sbase + kSX;
     const int64_t n_chunks = ceil_div(N, kTR);
     const Plan pl = plan_view(ws, n_chunks);
     const int tid = threadIdx.x;
     const int64_t slot_elems = int64_t(kTD) * kTD;
 
-    for (int64_t u = blockIdx.x; u < n_chunks * H; u += gridDim.x) {
-        const int64_t c = u / H;
+    const int64_t n_units = int64_t(pl.counters[3]) * H;
+    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const int64_t c = pl.active[u / H];
         const int h = int(u % H);
         const ChunkMeta m = pl.meta[c];
         const int fc = pl.first_cut[c];
@@ -284,7 +295,7 @@ state_tail_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         const unsigned long long cut = m.start | ~m.valid;
         // the carried segment (rank rb - 1) ends here: the chunk kernel stored its state
         const bool tail = fin != nullptr && fc > 0 && (fc < kTR || next_cut) && rb - 1 < n_state;
-        // segments starting here with a slot: a read-out of their initial state, and their
+        // segments starting here with a slot: the outputs of their rows here, and their
         // final state if they end here
         unsigned long long work = 0;
         {
@@ -304,18 +315,20 @@ state_tail_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
         __syncthreads();                          // the previous unit's reads are done
         const int64_t p0 = c * kTR;
         {
-            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            // all 64 rows of q, k, v and g in flight at once (16-byte asynchronous copies;
+            // rows past the end are zero-filled), beta alongside
             const __nv_bfloat16* src[4] = {q, k, v, g};
             const uint32_t dst[4] = {kSq, kSk, kSv, kSW};
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
-                for (int idx = tid; idx < kTR * 16; idx += kTailThreads) {
+#pragma unroll
+                for (int mm = 0; mm < kTR * 16 / kTailThreads; ++mm) {
+                    const int idx = tid + mm * kTailThreads;
                     const int i = idx >> 4, part = idx & 15;
                     const int64_t p = p0 + i;
-                    uint4 val = z;
-                    if (p < N)
-                        val = __ldg(reinterpret_cast<const uint4*>(src[a] + (p * H + h) * kTD) + part);
-                    reinterpret_cast<uint4*>(sm + dst[a])[idx] = val;
+                    const bool in = p < N;
+                    cp_async16(sbase + dst[a] + idx * 16,
+                               src[a] + ((in ? p : 0) * H + h) * kTD + part * 8, in ? 16u : 0u);
                 }
             }
             if (tid < kTR) {
@@ -323,15 +336,27 @@ state_tail_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                 reinterpret_cast<float*>(sm + kSB)[tid] =
                     p < N ? __bfloat162float(beta[p * H + h]) : 0.f;
             }
+            cp_async_wait_all();
         }
         __syncthreads();
-        if (tid < kTD) {                          // G, one key channel per thread
+        {                                         // G: four threads per key channel, 16 rows each
             const __nv_bfloat16* gs = reinterpret_cast<const __nv_bfloat16*>(sm + kSW);
             float* G = reinterpret_cast<float*>(sm + kSG);
+            float* qsum = reinterpret_cast<float*>(sm + kSQ);
+            const int ch = tid & (kTD - 1), qd = tid >> 7;
             float run = 0.f;
-            for (int i = 0; i < kTR; ++i) {
-                if ((m.valid >> i) & 1ull) run += __bfloat162float(gs[i * kTD + tid]);
-                G[i * kTD + tid] = run;
+#pragma unroll 8
+            for (int i = 16 * qd; i < 16 * qd + 16; ++i) {
+                if ((m.valid >> i) & 1ull) run += __bfloat162float(gs[i * kTD + ch]);
+                G[i * kTD + ch] = run;
+            }
+            qsum[qd * kTD + ch] = run;
+            __syncthreads();
+            float before = 0.f;
+            for (int q2 = 0; q2 < qd; ++q2) before += qsum[q2 * kTD + ch];
+            if (qd > 0) {
+#pragma unroll 8
+                for (int i = 16 * qd; i < 16 * qd + 16; ++i) G[i * kTD + ch] += before;
             }
         }
         __syncthreads();
@@ -348,9 +373,9 @@ state_tail_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
             const unsigned long long after = (r >= 63) ? 0ull : (cut & (~0ull << (r + 1)));
             const int end = after ? __ffsll((long long)after) - 1 : kTR;
             const float* S0 = init ? init + (rank * H + h) * slot_elems : nullptr;
-            if (S0) head_output<To>(t, r, end, S0, o, p0, H, h, scale);
             if (fin && (after != 0ull || next_cut))
                 final_state(t, r, end - 1, S0, fin + (rank * H + h) * slot_elems);
+            if (S0) head_output<To>(t, r, end, S0, o, p0, H, h, scale);
         }
     }
 }

@@ -89,11 +89,12 @@ def chunk_flops_per_token_head(wl: synth.Workload) -> int:
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one chunk-kernel
 # launch on the ling3 workload, from an ncu capture of
 # `python bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline`. It holds only
-# for the kernel sources it was taken on (SHA-1 over the two files below);
+# for the kernel sources it was taken on (SHA-1 over the three files below);
 # after any change to them the bench reports null until a new capture.
-CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "72e497cd3dc01b03ae2c67a07e2596f30cdf6e29",
-                 "read": 558_211_840, "write": 118_858_240}
-CHUNK_SOURCES = ("kda_segids_cu_gb300/csrc/kda_chunk_tc.cu", "kda_segids_cu_gb300/csrc/kda_sm100.cuh")
+CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "61633d169bf9c66c0c88b2bf3139130e19f793d7",
+                 "read": 558_069_248, "write": 117_980_672}
+CHUNK_SOURCES = ("kda_segids_cu_gb300/csrc/kda_chunk_tc.cu", "kda_segids_cu_gb300/csrc/kda_sm100.cuh",
+                 "kda_segids_cu_gb300/csrc/kda_plan.cuh")
 
 
 def chunk_traffic(wl: synth.Workload):

@@ -211,3 +211,29 @@ def test_tensor_core_chaining():
     o_c, f_c = _run(inp, 1, T, torch.cat([init, f_a[:1].cpu()]), 2, seg=cut)
     check_kda_output(o_c, ref, whole, torch.bfloat16, label="chained")
     _check_states(f_c[1:], ref_fin, "chained")
+
+
+@pytest.mark.parametrize("name,heads", [("ling3", [0, 9]), ("short", [3]), ("long", [0, 31])])
+def test_large_workloads_state_sampled_heads(name, heads):
+    """Full-size workloads in bench.py's configuration (every segment with an initial and
+    a final state), held to the oracle on sampled heads: outputs on every token of those
+    heads, final states of every segment."""
+    wl = synth.WORKLOADS[name]
+    inp = synth.make_kda_inputs(wl, device="cuda")
+    seg = inp.segment_ids
+    n = _n_segments(seg.cpu() if seg is not None else None, wl.B)
+    H, D = wl.H, wl.d_qk
+    gen = torch.Generator(device="cuda").manual_seed(17)
+    init = torch.randn(n, H, D, D, device="cuda", generator=gen) * 0.1
+    o, fin = kda.kda_chunk_fwd_varlen_state(inp.q, inp.k, inp.v, inp.g, inp.beta, seg, B=wl.B,
+                                            T=wl.T, initial_state=init, output_final_state=True)
+    torch.cuda.synchronize()
+    hs = torch.tensor(heads, device="cuda")
+    pick = lambda t: t.index_select(1, hs).cpu()     # noqa: E731
+    ref, ref_fin = oracle.kda_fwd_state(pick(inp.q), pick(inp.k), pick(inp.v), pick(inp.g),
+                                        pick(inp.beta), None if seg is None else seg.cpu(),
+                                        wl.B, wl.T, initial_state=pick(init), n_state=n,
+                                        want_final=True)
+    check_kda_output(o, ref, None if seg is None else seg.cpu(), wl.dtype, heads=heads,
+                     label=name)
+    _check_states(pick(fin), ref_fin, name)

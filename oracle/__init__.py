@@ -12,10 +12,16 @@ The arithmetic lives in ``kda_oracle.c`` (plain C, fp64), built with gcc into
   short_conv(x, w, seg, out_dtype)     RFC-0025 方案 §3
   kda_fwd(q, k, v, g, beta, seg, ...)  RFC-0026 背景 "KDA 状态泄漏问题" and
                                        §3.1.1 reset semantics
+  kda_fwd_state(...)                   the same with per-segment initial and
+                                       final states (RFC-0026's kwargs)
+  kda_bwd(q, k, v, g, beta, do, seg)   gradients of kda_fwd, by reverse-mode
+                                       differentiation of the recurrence
 
 Parity pins live in tests/test_oracle_*.py. Parity status of each function:
-cu_seqlens, short_conv and kda_fwd are all pinned (worked examples from the
-page, library routines, closed forms, brute force and invariants).
+cu_seqlens, short_conv, kda_fwd and kda_fwd_state are pinned (worked examples
+from the page, library routines, closed forms, brute force and invariants);
+kda_bwd is pinned by finite differences of kda_fwd and by automatic
+differentiation of the brute-force closed form.
 """
 from __future__ import annotations
 
@@ -64,6 +70,9 @@ def _load():
             lib.oracle_kda_fwd_state.argtypes = [dp, dp, dp, dp, dp, ip, i64, i64, i64, i64, i64,
                                                  ctypes.c_double, dp, dp, i64, dp, ctypes.c_int]
             lib.oracle_kda_fwd_state.restype = ctypes.c_int
+            lib.oracle_kda_bwd.argtypes = [dp, dp, dp, dp, dp, ip, i64, i64, i64, i64, i64,
+                                           ctypes.c_double, dp, dp, dp, dp, dp, dp, ctypes.c_int]
+            lib.oracle_kda_bwd.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -190,3 +199,39 @@ def kda_fwd_state(q, k, v, g, beta, seg=None, B: int | None = None, T: int | Non
         raise ValueError("oracle_kda_fwd_state: bad arguments")
     fin = torch.from_numpy(fa).to(out_dtype) if fa is not None else None
     return torch.from_numpy(o).to(out_dtype), fin
+
+
+def kda_bwd(q, k, v, g, beta, d_o, seg=None, B: int | None = None, T: int | None = None,
+            scale: float = 1.0, n_threads: int | None = None, out_dtype=torch.float64):
+    """Gradients of kda_fwd with respect to q, k, v, g and beta for the upstream
+    gradient d_o ([B*T, H, Dv]). Returns (dq, dk, dv, dg, dbeta), float64 unless
+    out_dtype says otherwise; all zero on padding tokens."""
+    qa, ka, va, ga, da = (_np(t, np.float64) for t in (q, k, v, g, d_o))
+    ba = _np(beta, np.float64)
+    if seg is not None:
+        sa = _np(seg, np.int32)
+        if sa.ndim == 1:
+            sa = sa[None, :]
+        if B is None:
+            B, T = sa.shape
+        sa = sa.reshape(B, T)
+    else:
+        sa = None
+        if B is None:
+            B, T = 1, qa.reshape(-1, *qa.shape[-2:]).shape[0]
+    Dk, Dv = qa.shape[-1], va.shape[-1]
+    H = qa.shape[-2]
+    N = B * T
+    qa, ka, ga = (a.reshape(N, H, Dk) for a in (qa, ka, ga))
+    va, da = va.reshape(N, H, Dv), da.reshape(N, H, Dv)
+    ba = ba.reshape(N, H)
+    dq, dk, dg = (np.zeros((N, H, Dk)) for _ in range(3))
+    dv = np.zeros((N, H, Dv))
+    db = np.zeros((N, H))
+    nt = default_threads() if n_threads is None else n_threads
+    rc = _load().oracle_kda_bwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), _ptr(ba), _ptr(sa), B, T,
+                                H, Dk, Dv, float(scale), _ptr(da), _ptr(dq), _ptr(dk), _ptr(dv),
+                                _ptr(dg), _ptr(db), int(nt))
+    if rc != 0:
+        raise ValueError("oracle_kda_bwd: bad arguments or out of memory")
+    return tuple(torch.from_numpy(a).to(out_dtype) for a in (dq, dk, dv, dg, db))

@@ -211,28 +211,15 @@ static void *kda_worker(void *arg)
 }
 
 /*
- * Splits every row into its segments (maximal runs of equal non-zero ids,
- * cut at row starts), zeroes o, and runs one independent recurrence per
- * (segment, head) on `n_threads` threads. Starting each segment from S = 0
- * is exactly the reset rule above.
- *
- * Per-segment state ([RFC-0026] 方案, the kernel kwargs initial_state and
- * output_final_state of the FLA chunk_kda call; shapes [n_segments, H, Dk, Dv]):
- * segment r, counted in flattened token order, starts from init[r] instead of
- * zero when init is given and r < n_state, and its state after its last token
- * is written to fin[r] when fin is given and r < n_state. With init = NULL this
- * is the reset rule above. Returns 0, or -1 on bad arguments.
+ * The (segment, head) work units of a packed batch: every row split into its
+ * segments (maximal runs of equal non-zero ids, cut at row starts), each as
+ * (row, head, first token, one-past-last token, segment rank), ranks counted in
+ * flattened token order. Returns a malloc'd array of 5 * n_units entries, or
+ * NULL if out of memory.
  */
-int oracle_kda_fwd_state(const double *q, const double *k, const double *v, const double *g,
-                         const double *beta, const int32_t *seg, int64_t B, int64_t T, int64_t H,
-                         int64_t Dk, int64_t Dv, double scale, const double *init, double *fin,
-                         int64_t n_state, double *o, int n_threads)
+static int64_t *segment_units(const int32_t *seg, int64_t B, int64_t T, int64_t H,
+                              int64_t *n_units_out)
 {
-    if (!q || !k || !v || !g || !beta || !o || B < 0 || T < 0 || H < 1 || Dk < 1 || Dv < 1 ||
-        n_state < 0)
-        return -1;
-    const int64_t N = B * T;
-    memset(o, 0, sizeof(double) * (size_t)(N * H * Dv));
     /* count segments */
     int64_t n_seg = 0;
     for (int64_t b = 0; b < B; ++b)
@@ -244,7 +231,7 @@ int oracle_kda_fwd_state(const double *q, const double *k, const double *v, cons
         }
     int64_t *units = (int64_t *)malloc(sizeof(int64_t) * 5 * (size_t)(n_seg * H + 1));
     if (!units)
-        return -1;
+        return NULL;
     int64_t n_units = 0;
     int64_t rank = 0; /* segments in flattened token order */
     for (int64_t b = 0; b < B; ++b) {
@@ -271,6 +258,37 @@ int oracle_kda_fwd_state(const double *q, const double *k, const double *v, cons
             t = e;
         }
     }
+    *n_units_out = n_units;
+    return units;
+}
+
+/*
+ * Splits every row into its segments (maximal runs of equal non-zero ids,
+ * cut at row starts), zeroes o, and runs one independent recurrence per
+ * (segment, head) on `n_threads` threads. Starting each segment from S = 0
+ * is exactly the reset rule above.
+ *
+ * Per-segment state ([RFC-0026] 方案, the kernel kwargs initial_state and
+ * output_final_state of the FLA chunk_kda call; shapes [n_segments, H, Dk, Dv]):
+ * segment r, counted in flattened token order, starts from init[r] instead of
+ * zero when init is given and r < n_state, and its state after its last token
+ * is written to fin[r] when fin is given and r < n_state. With init = NULL this
+ * is the reset rule above. Returns 0, or -1 on bad arguments.
+ */
+int oracle_kda_fwd_state(const double *q, const double *k, const double *v, const double *g,
+                         const double *beta, const int32_t *seg, int64_t B, int64_t T, int64_t H,
+                         int64_t Dk, int64_t Dv, double scale, const double *init, double *fin,
+                         int64_t n_state, double *o, int n_threads)
+{
+    if (!q || !k || !v || !g || !beta || !o || B < 0 || T < 0 || H < 1 || Dk < 1 || Dv < 1 ||
+        n_state < 0)
+        return -1;
+    const int64_t N = B * T;
+    memset(o, 0, sizeof(double) * (size_t)(N * H * Dv));
+    int64_t n_units = 0;
+    int64_t *units = segment_units(seg, B, T, H, &n_units);
+    if (!units)
+        return -1;
     kda_job_t J = {q, k, v, g, beta, seg, B, T, H, Dk, Dv, scale, o,
                    init, fin, n_state, units, n_units, 0};
     if (n_threads < 1)
@@ -301,4 +319,158 @@ int oracle_kda_fwd(const double *q, const double *k, const double *v, const doub
 {
     return oracle_kda_fwd_state(q, k, v, g, beta, seg, B, T, H, Dk, Dv, scale, NULL, NULL, 0, o,
                                 n_threads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* O4: gradients of the recurrence                                           */
+/* ------------------------------------------------------------------------ */
+/*
+ * The pages state the forward only; its gradients follow by differentiating
+ * the recurrence above step by step in reverse (reverse-mode automatic
+ * differentiation written out by hand). For a loss L with dL/do_t = do_t,
+ * per (segment, head), keeping the forward states S_t and with S = 0 before
+ * the segment's first token, going backwards over t with A = dL/dS_t (A = 0
+ * after the segment's last token):
+ *     A       += scale * q_t (x) do_t                 (o_t = scale S_t^T q_t)
+ *     dq_t     = scale * S_t do_t
+ *     dbeta_t  = k_t^T A v_t                            (S_t = S'_t + beta_t k_t v_t^T)
+ *     dk_t     = beta_t * A v_t
+ *     dv_t     = beta_t * A^T k_t
+ *     dg_t[i]  = exp(g_t[i]) * sum_j A[i][j] S_{t-1}[i][j]   (S'_t = S_{t-1} exp(g_t))
+ *     A[i][j] *= exp(g_t[i])                            (A becomes dL/dS_{t-1})
+ * Padding tokens get zero gradients (they take no part in the forward).
+ */
+typedef struct {
+    const double *q, *k, *v, *g, *beta, *d_o;
+    int64_t T, H, Dk, Dv;
+    double scale;
+    double *dq, *dk, *dv, *dg, *dbeta;
+    const int64_t *units;
+    int64_t n_units;
+    int64_t next;   /* shared counter */
+    int failed;     /* set when a unit could not get its memory */
+} kda_bwd_job_t;
+
+static void run_bwd_unit(kda_bwd_job_t *J, int64_t b, int64_t h, int64_t t0, int64_t t1)
+{
+    const int64_t H = J->H, Dk = J->Dk, Dv = J->Dv, L = t1 - t0, DD = Dk * Dv;
+    /* states[0] = S before the first token (zero), states[1 + u] = S after token t0 + u */
+    double *states = (double *)calloc((size_t)((L + 1) * DD), sizeof(double));
+    double *A = (double *)calloc((size_t)DD, sizeof(double));
+    if (!states || !A) {
+        free(states);
+        free(A);
+        __atomic_store_n(&J->failed, 1, __ATOMIC_RELAXED);
+        return;
+    }
+    for (int64_t u = 0; u < L; ++u) {             /* forward, keeping every state */
+        const int64_t row = (b * J->T + t0 + u) * H + h;   /* (token, head) */
+        const double *kt = J->k + row * Dk;
+        const double *gt = J->g + row * Dk;
+        const double *vt = J->v + row * Dv;
+        const double bt = J->beta[row];
+        const double *prev = states + u * DD;
+        double *cur = states + (u + 1) * DD;
+        for (int64_t i = 0; i < Dk; ++i)
+            for (int64_t j = 0; j < Dv; ++j)
+                cur[i * Dv + j] = prev[i * Dv + j] * exp(gt[i]) + bt * kt[i] * vt[j];
+    }
+    for (int64_t u = L - 1; u >= 0; --u) {        /* backward */
+        const int64_t row = (b * J->T + t0 + u) * H + h;
+        const double *qt = J->q + row * Dk;
+        const double *kt = J->k + row * Dk;
+        const double *gt = J->g + row * Dk;
+        const double *vt = J->v + row * Dv;
+        const double *dot = J->d_o + row * Dv;
+        const double bt = J->beta[row];
+        const double *S = states + (u + 1) * DD;      /* S_t */
+        const double *Sp = states + u * DD;           /* S_{t-1} */
+        double *dqt = J->dq + row * Dk;
+        double *dkt = J->dk + row * Dk;
+        double *dvt = J->dv + row * Dv;
+        double *dgt = J->dg + row * Dk;
+        for (int64_t i = 0; i < Dk; ++i)
+            for (int64_t j = 0; j < Dv; ++j)
+                A[i * Dv + j] += J->scale * qt[i] * dot[j];
+        double db = 0.0;
+        for (int64_t i = 0; i < Dk; ++i) {
+            double sq = 0.0, av = 0.0, sg = 0.0;
+            for (int64_t j = 0; j < Dv; ++j) {
+                sq += S[i * Dv + j] * dot[j];
+                av += A[i * Dv + j] * vt[j];
+                sg += A[i * Dv + j] * Sp[i * Dv + j];
+            }
+            dqt[i] = J->scale * sq;
+            dkt[i] = bt * av;
+            dgt[i] = exp(gt[i]) * sg;
+            db += kt[i] * av;
+        }
+        for (int64_t j = 0; j < Dv; ++j) {
+            double ak = 0.0;
+            for (int64_t i = 0; i < Dk; ++i)
+                ak += A[i * Dv + j] * kt[i];
+            dvt[j] = bt * ak;
+        }
+        J->dbeta[row] = db;
+        for (int64_t i = 0; i < Dk; ++i)
+            for (int64_t j = 0; j < Dv; ++j)
+                A[i * Dv + j] *= exp(gt[i]);
+    }
+    free(states);
+    free(A);
+}
+
+static void *kda_bwd_worker(void *arg)
+{
+    kda_bwd_job_t *J = (kda_bwd_job_t *)arg;
+    for (;;) {
+        const int64_t u = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
+        if (u >= J->n_units)
+            break;
+        const int64_t *U = J->units + 5 * u;
+        run_bwd_unit(J, U[0], U[1], U[2], U[3]);
+    }
+    return NULL;
+}
+
+/*
+ * Gradients of the forward above (no per-segment state) for upstream gradient
+ * d_o: dq, dk, dg [B*T, H, Dk], dv [B*T, H, Dv], dbeta [B*T, H], all written
+ * (zero on padding). One independent reverse pass per (segment, head) on
+ * `n_threads` threads. Returns 0, or -1 on bad arguments or out of memory.
+ */
+int oracle_kda_bwd(const double *q, const double *k, const double *v, const double *g,
+                   const double *beta, const int32_t *seg, int64_t B, int64_t T, int64_t H,
+                   int64_t Dk, int64_t Dv, double scale, const double *d_o, double *dq,
+                   double *dk, double *dv, double *dg, double *dbeta, int n_threads)
+{
+    if (!q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta || B < 0 ||
+        T < 0 || H < 1 || Dk < 1 || Dv < 1)
+        return -1;
+    const int64_t N = B * T;
+    memset(dq, 0, sizeof(double) * (size_t)(N * H * Dk));
+    memset(dk, 0, sizeof(double) * (size_t)(N * H * Dk));
+    memset(dg, 0, sizeof(double) * (size_t)(N * H * Dk));
+    memset(dv, 0, sizeof(double) * (size_t)(N * H * Dv));
+    memset(dbeta, 0, sizeof(double) * (size_t)(N * H));
+    int64_t n_units = 0;
+    int64_t *units = segment_units(seg, B, T, H, &n_units);
+    if (!units)
+        return -1;
+    kda_bwd_job_t J = {q, k, v, g, beta, d_o, T, H, Dk, Dv, scale,
+                       dq, dk, dv, dg, dbeta, units, n_units, 0, 0};
+    if (n_threads < 1)
+        n_threads = 1;
+    if (n_threads > 256)
+        n_threads = 256;
+    pthread_t th[256];
+    int started = 0;
+    for (int i = 1; i < n_threads; ++i)
+        if (pthread_create(&th[started], NULL, kda_bwd_worker, &J) == 0)
+            ++started;
+    kda_bwd_worker(&J);
+    for (int i = 0; i < started; ++i)
+        pthread_join(th[i], NULL);
+    free(units);
+    return J.failed ? -1 : 0;
 }

@@ -30,6 +30,14 @@ MUTATIONS = {
     # per-segment state
     "initial_state_ignored": ("if (J->init && r < J->n_state)", "if (0 && J->init && r < J->n_state)"),
     "state_rank_off_by_one": ("units[5 * n_units + 4] = rank;", "units[5 * n_units + 4] = rank + 1;"),
+    # gradients
+    "bwd_no_adjoint_decay": ("                A[i * Dv + j] *= exp(gt[i]);",
+                             "                A[i * Dv + j] *= 1.0;"),
+    "bwd_dg_current_state": ("sg += A[i * Dv + j] * Sp[i * Dv + j];",
+                             "sg += A[i * Dv + j] * S[i * Dv + j];"),
+    "bwd_dq_no_scale": ("dqt[i] = J->scale * sq;", "dqt[i] = sq;"),
+    "bwd_dv_uses_q": ("ak += A[i * Dv + j] * kt[i];", "ak += A[i * Dv + j] * qt[i];"),
+    "bwd_dbeta_dropped_k": ("db += kt[i] * av;", "db += av;"),
     # conv
     "conv_tap_forward": ("const int64_t s = t - j;", "const int64_t s = t - (K - 1 - j);"),
     "conv_no_mask": ("if (seg && seg[b * T + s] != seg[b * T + t])", "if (0)"),
@@ -64,10 +72,13 @@ def _pins_pass(monkeypatch, so_path) -> bool:
                                    ctypes.c_double, vp, ctypes.c_int]
     lib.oracle_kda_fwd_state.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                          ctypes.c_double, vp, vp, i64, vp, ctypes.c_int]
+    lib.oracle_kda_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                   ctypes.c_double, vp, vp, vp, vp, vp, vp, ctypes.c_int]
     monkeypatch.setattr(oracle, "_lib", lib)
     import tests.test_oracle_cu_seqlens as tc
     import tests.test_oracle_conv as tv
     import tests.test_oracle_kda as tk
+    import tests.test_oracle_bwd as tb
     import tests.test_oracle_state as ts
     golden = os.path.join(os.path.dirname(tc.__file__), "golden")
     checks = [
@@ -86,6 +97,8 @@ def _pins_pass(monkeypatch, so_path) -> bool:
         lambda: ts.test_closed_forms_bruteforce(),
         lambda: ts.test_chaining_identity(),
         lambda: ts.test_state_slots_beyond_n_state_and_ranks(),
+        lambda: tb.test_finite_differences(),
+        lambda: tb.test_autograd_of_closed_form(),
     ]
     for c in checks:
         try:

@@ -366,6 +366,31 @@ def run_gb300(args):
         torch.cuda.synchronize()
         state_ms = sa.elapsed_time(sb) / n_rep
 
+    # ---- gradients (kda_chunk_bwd_varlen) for a random upstream gradient, timed apart ----
+    do_gen = torch.Generator(device=dev).manual_seed(13)
+    d_o = torch.randn(kin.v.shape, device=dev, generator=do_gen).to(kin.v.dtype)
+    bwd_ws = torch.empty(max(256, int(kda.load_library().kda_chunk_bwd_varlen_workspace_size(
+        wl.B, wl.T, H, wl.d_qk, wl.d_v, 1 if kin.q.dtype == torch.bfloat16 else 0))),
+        dtype=torch.uint8, device=dev)
+    bwd_out = None
+
+    def bwd_call():
+        return kda.kda_chunk_bwd_varlen(kin.q, kin.k, kin.v, kin.g, kin.beta, d_o, seg, B=wl.B,
+                                        T=wl.T, workspace=bwd_ws)
+
+    bwd_out = bwd_call()
+    torch.cuda.synchronize()
+    ba = torch.cuda.Event(enable_timing=True)
+    bb = torch.cuda.Event(enable_timing=True)
+    n_bwd = 3
+    ba.record(stream)
+    for _ in range(n_bwd):
+        bwd_out = bwd_call()
+    bb.record(stream)
+    torch.cuda.synchronize()
+    bwd_ms = ba.elapsed_time(bb) / n_bwd
+    del bwd_out, bwd_ws
+
     # ---- e2e through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
@@ -484,7 +509,10 @@ def run_gb300(args):
                 ("kda_short_conv_varlen", conv_ms, 2 * N * wl.F * convs[0].x.element_size()),
                 ("kda_chunk_fwd_varlen", chunk_ms, bytes_launch),
                 ("kda_chunk_fwd_varlen_state", state_ms,
-                 bytes_launch + 2 * n_state * H * wl.d_qk * wl.d_v * 4))
+                 bytes_launch + 2 * n_state * H * wl.d_qk * wl.d_v * 4),
+                # reads q, k, g, v, beta, d_o; writes dq, dk, dg, dv, dbeta
+                ("kda_chunk_bwd_varlen", bwd_ms,
+                 N * H * (6 * wl.d_qk + 4 * wl.d_v + 2) * kin.q.element_size()))
             if ms_ is not None
         },
         "real_tokens_per_s": real_tokens * ws / (ms / 1e3),

@@ -200,6 +200,49 @@ kda_status_t kda_chunk_fwd_varlen_state(const void *q, const void *k, const void
                                         uint32_t *status_dev, kda_stream_t stream);
 
 /*
+ * kda_chunk_bwd_varlen_workspace_size -- bytes of device scratch that
+ * kda_chunk_bwd_varlen needs (0 on invalid or unsupported sizes): the segment
+ * list, dq in fp32 and one fp32 state per 64-token chunk and head, about
+ * (B*T) * H * (4 d_qk + 4 d_qk d_v / 64) bytes.
+ */
+size_t kda_chunk_bwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int32_t d_qk,
+                                           int32_t d_v, kda_dtype_t dtype);
+
+/*
+ * kda_chunk_bwd_varlen -- gradients of kda_chunk_fwd_varlen (no per-segment
+ * state) with respect to q, k, v, g and beta, for an upstream gradient d_o of o.
+ * The pages state the forward only; these are its derivatives:
+ *     A_t     = dL/dS_t = scale q_t d_o_t^T + exp(g_{t+1}) * A_{t+1}
+ *               (rows scaled; zero past a segment's last token)
+ *     dq_t    = scale S_t d_o_t
+ *     dk_t    = beta_t A_t v_t      dv_t = beta_t A_t^T k_t
+ *     dbeta_t = k_t^T A_t v_t
+ *     dg_t    = sum over the segment's tokens u >= t of (q_u * dq_u - k_u * dk_u)
+ * Padding tokens get zero gradients. The running sum for dg restarts at every
+ * 64-token chunk start from its direct form exp(g_t) * sum_j A_t[i][j] S_{t-1}[i][j]
+ * (the sum cancels, so its rounding error would otherwise grow with the segment).
+ *
+ * Layout and arguments are those of kda_chunk_fwd_varlen, with the workspace size
+ * from kda_chunk_bwd_varlen_workspace_size, plus:
+ *   d_o          device [B*T, H, d_v] of `dtype`
+ *   dq, dk, dg   device [B*T, H, d_qk] of `grad_dtype`
+ *   dv           device [B*T, H, d_v] of `grad_dtype`
+ *   dbeta        device [B*T, H] of `grad_dtype`
+ *   grad_dtype   KDA_F32, or equal to `dtype`; values rounded once to nearest even
+ * It runs in fp32 arithmetic as two walks per (segment, head): forward for dq
+ * and the chunk-start states, then backward for the rest, which reads them back.
+ *
+ * Returns KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE or
+ * KDA_ERR_CUDA. Calls that share a workspace must not overlap in time.
+ */
+kda_status_t kda_chunk_bwd_varlen(const void *q, const void *k, const void *v, const void *g,
+                                  const void *beta, const int32_t *segment_ids, int64_t B,
+                                  int64_t T, int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                  kda_dtype_t dtype, const void *d_o, kda_dtype_t grad_dtype,
+                                  void *dq, void *dk, void *dv, void *dg, void *dbeta,
+                                  void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_varlen_noalloc -- kda_chunk_fwd_varlen for callers that cannot
  * allocate device memory. The pages have no counterpart: this is a calling
  * convention of this library, not part of the method.

@@ -65,6 +65,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                                ctypes.c_float, ctypes.c_int, ctypes.c_int, vp,
                                                vp, vp, i64, vp, ctypes.c_size_t, u32p, vp]
     lib.kda_chunk_fwd_varlen_state.restype = ctypes.c_int
+    lib.kda_chunk_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32,
+                                         ctypes.c_float, ctypes.c_int, vp, ctypes.c_int, vp, vp,
+                                         vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.kda_chunk_bwd_varlen.restype = ctypes.c_int
+    lib.kda_chunk_bwd_varlen_workspace_size.argtypes = [i64, i64, i32, i32, i32, ctypes.c_int]
+    lib.kda_chunk_bwd_varlen_workspace_size.restype = ctypes.c_size_t
     if path is None:
         _lib = lib
     return lib
@@ -152,8 +158,11 @@ def chunk_fwd_workspace_bytes(B: int, T: int, H: int, d_qk: int, d_v: int, dtype
                                                                   _dtype_code(dtype)))
 
 
-def _chunk_args(q, k, v, g, beta, segment_ids, B, T, out, workspace, out_dtype):
-    """Checks and marshals the arguments the chunk entry points share."""
+def _chunk_args(q, k, v, g, beta, segment_ids, B, T, out, workspace, out_dtype,
+                workspace_size=None, want_out=True):
+    """Checks and marshals the arguments the chunk entry points share; allocates o (if
+    want_out) and the workspace (workspace_size(B, T, H, Dk, Dv, dtype code) bytes, by
+    default the forward's) when they are not given."""
     q, k, v, g, beta = (_dev(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (g, "g"),
                                                  (beta, "beta")))
     H, Dk = q.shape[-2], q.shape[-1]
@@ -185,9 +194,14 @@ def _chunk_args(q, k, v, g, beta, segment_ids, B, T, out, workspace, out_dtype):
         if out.numel() != v.numel() or not out.is_contiguous():
             raise ValueError("out must be a contiguous tensor with v's element count")
     odt = _dtype_code(out_dtype)
-    o = out if out is not None else torch.empty(v.shape, dtype=out_dtype, device=v.device)
-    need = chunk_fwd_workspace_bytes(B, T, H, Dk, Dv, q.dtype)
+    o = None
+    if want_out:
+        o = out if out is not None else torch.empty(v.shape, dtype=out_dtype, device=v.device)
     if workspace is None:
+        if workspace_size is None:
+            need = chunk_fwd_workspace_bytes(B, T, H, Dk, Dv, q.dtype)
+        else:
+            need = int(workspace_size(B, T, H, Dk, Dv, dt))
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     return q, k, v, g, beta, seg, B, T, H, Dk, Dv, dt, odt, o, workspace
 
@@ -248,7 +262,57 @@ def kda_chunk_fwd_varlen_state(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
     return o, fin
 
 
+def kda_chunk_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                         beta: torch.Tensor, d_o: torch.Tensor,
+                         segment_ids: torch.Tensor | None = None, scale: float = 1.0,
+                         B: int | None = None, T: int | None = None, stream=None,
+                         workspace: torch.Tensor | None = None,
+                         grad_dtype: torch.dtype | None = None):
+    """Gradients of kda_chunk_fwd_varlen for the upstream gradient d_o (shaped like v, of
+    the input dtype). Returns (dq, dk, dv, dg, dbeta) shaped like q, k, v, g, beta, of
+    `grad_dtype` (default: the input dtype; float32 is also accepted)."""
+    q, k, v, g, beta, seg, B, T, H, Dk, Dv, dt, _, _, workspace = _chunk_args(
+        q, k, v, g, beta, segment_ids, B, T, None, workspace, None,
+        workspace_size=load_library().kda_chunk_bwd_varlen_workspace_size, want_out=False)
+    d_o = _dev(d_o, "d_o")
+    if d_o.numel() != v.numel() or d_o.dtype != q.dtype:
+        raise ValueError("d_o must be shaped like v, of the input dtype")
+    grad_dtype = q.dtype if grad_dtype is None else grad_dtype
+    gdt = _dtype_code(grad_dtype)
+    dq, dk, dv, dg, db = (torch.empty(t.shape, dtype=grad_dtype, device=q.device)
+                          for t in (q, k, v, g, beta))
+    _check("kda_chunk_bwd_varlen",
+           load_library().kda_chunk_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                               _ptr(seg), B, T, H, Dk, Dv, float(scale), dt,
+                                               _ptr(d_o), gdt, _ptr(dq), _ptr(dk), _ptr(dv),
+                                               _ptr(dg), _ptr(db), _ptr(workspace),
+                                               workspace.numel(), _stream_ptr(stream)))
+    return dq, dk, dv, dg, db
+
+
+class _KdaVarlen(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, segment_ids, scale, B, T):
+        ctx.save_for_backward(q, k, v, g, beta, segment_ids)
+        ctx.scale, ctx.B, ctx.T = scale, B, T
+        return kda_chunk_fwd_varlen(q, k, v, g, beta, segment_ids, scale=scale, B=B, T=T)
+
+    @staticmethod
+    def backward(ctx, d_o):
+        q, k, v, g, beta, seg = ctx.saved_tensors
+        grads = kda_chunk_bwd_varlen(q, k, v, g, beta, d_o.contiguous(), seg, scale=ctx.scale,
+                                     B=ctx.B, T=ctx.T)
+        return (*grads, None, None, None, None)
+
+
+def kda_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+               beta: torch.Tensor, segment_ids: torch.Tensor | None = None, scale: float = 1.0,
+               B: int | None = None, T: int | None = None) -> torch.Tensor:
+    """kda_chunk_fwd_varlen as a differentiable op: its backward runs kda_chunk_bwd_varlen."""
+    return _KdaVarlen.apply(q, k, v, g, beta, segment_ids, scale, B, T)
+
+
 __all__ = ["kda_segids_to_cu_seqlens", "kda_short_conv_varlen", "kda_chunk_fwd_varlen",
-           "kda_chunk_fwd_varlen_state",
+           "kda_chunk_fwd_varlen_state", "kda_chunk_bwd_varlen", "kda_varlen",
            "chunk_fwd_workspace_bytes", "load_library", "header_functions", "KdaError",
            "KDA_DEV_DECAY_RANGE"]

@@ -19,6 +19,12 @@ kda_status_t launch_chunk_tc(const void* q, const void* k, const void* v, const 
                              int32_t H, int32_t D, float scale, kda_dtype_t out_dtype, void* o,
                              void* ws, uint32_t* status_dev, const float* init, float* fin,
                              int64_t n_state, cudaStream_t stream);
+size_t bwd_workspace_bytes(int64_t N, int32_t H, int32_t D);
+kda_status_t launch_bwd(const void* q, const void* k, const void* v, const void* g,
+                        const void* beta, const void* d_o, const int32_t* seg, int64_t B,
+                        int64_t T_len, int32_t H, int32_t D, float scale, kda_dtype_t dtype,
+                        kda_dtype_t grad_dtype, void* dq, void* dk, void* dv, void* dg,
+                        void* dbeta, void* ws, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -148,6 +154,39 @@ kda_status_t kda_chunk_fwd_varlen_state(const void* q, const void* k, const void
     return kda::launch_recurrent_state(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale, dtype,
                                        out_dtype, o, workspace, initial_state, final_state,
                                        n_state, st);
+}
+
+size_t kda_chunk_bwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int32_t d_qk,
+                                           int32_t d_v, kda_dtype_t dtype) {
+    if (!token_count_ok(B, T) || H < 1 || d_qk < 1 || d_v < 1 || !valid_dtype(dtype)) return 0;
+    if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return 0;
+    return kda::bwd_workspace_bytes(B * T, H, d_qk);
+}
+
+kda_status_t kda_chunk_bwd_varlen(const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const int32_t* segment_ids, int64_t B,
+                                  int64_t T, int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                  kda_dtype_t dtype, const void* d_o, kda_dtype_t grad_dtype,
+                                  void* dq, void* dk, void* dv, void* dg, void* dbeta,
+                                  void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    if (!q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta)
+        return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !valid_dtype(grad_dtype) || !token_count_ok(B, T) || H < 1 ||
+        d_qk < 1 || d_v < 1)
+        return KDA_ERR_INVALID_ARG;
+    if (grad_dtype != dtype && grad_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return KDA_ERR_UNSUPPORTED;
+    if (int64_t(H) * d_qk > 65536) return KDA_ERR_UNSUPPORTED;
+    const void* ptrs[] = {q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta};
+    for (const void* p : ptrs)
+        if (!kda::aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (segment_ids && !kda::aligned(segment_ids, 4)) return KDA_ERR_INVALID_ARG;
+    const size_t need = kda_chunk_bwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
+    if (!workspace || workspace_bytes < need || !kda::aligned(workspace, 256))
+        return KDA_ERR_WORKSPACE;
+    return kda::launch_bwd(q, k, v, g, beta, d_o, segment_ids, B, T, H, d_qk, scale, dtype,
+                           grad_dtype, dq, dk, dv, dg, dbeta, workspace,
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -294,6 +294,18 @@ size_t recurrent_workspace_bytes(int64_t N) {
     return size_t(N) * 8 + 256;
 }
 
+// The segment list in the first 8 N + 256 bytes of ws: seg_start[N], seg_end[N], counters.
+kda_status_t launch_segment_list(const int32_t* seg, int64_t B, int64_t T_len, void* ws,
+                                 cudaStream_t stream) {
+    const int64_t N = B * T_len;
+    int32_t* seg_start = static_cast<int32_t*>(ws);
+    int32_t* seg_end = seg_start + N;
+    int32_t* counters = seg_end + N;
+    list_segments_kernel<<<1, kListThreads, 0, stream>>>(seg, N, RowStartTest::make(T_len),
+                                                         seg_start, seg_end, counters);
+    return launch_status();
+}
+
 template <typename T, typename To>
 static kda_status_t launch_recurrent_typed(const void* q, const void* k, const void* v,
                                            const void* g, const void* beta, const int32_t* seg,
@@ -304,10 +316,7 @@ static kda_status_t launch_recurrent_typed(const void* q, const void* k, const v
     int32_t* seg_start = static_cast<int32_t*>(ws);
     int32_t* seg_end = seg_start + N;
     int32_t* counters = seg_end + N;
-    list_segments_kernel<<<1, kListThreads, 0, stream>>>(seg, N, RowStartTest::make(T_len),
-                                                         seg_start, seg_end,
-                                                         counters);
-    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    if (launch_segment_list(seg, B, T_len, ws, stream) != KDA_OK) return KDA_ERR_CUDA;
     if (seg != nullptr) {
         zero_padding_kernel<To><<<unsigned(N), 128, 0, stream>>>(seg, N, int64_t(H) * D,
                                                                  static_cast<To*>(o));

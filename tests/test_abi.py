@@ -113,3 +113,30 @@ def test_chunk_state_rejects_invalid_arguments(lib):
     assert call(dk=96, dv=96) == -2
     assert call(ws=None) == -4
     assert call(ws_bytes=ws - 1) == -4
+
+
+def test_chunk_bwd_rejects_invalid_arguments(lib):
+    f = lib.kda_chunk_bwd_varlen
+    ws = lib.kda_chunk_bwd_varlen_workspace_size(1, 64, 2, 64, 64, kda.KDA_BF16)
+    assert ws > 0
+    assert lib.kda_chunk_bwd_varlen_workspace_size(1, 64, 2, 96, 96, kda.KDA_BF16) == 0
+    args = [FAKE] * 5 + [None, 1, 64, 2, 64, 64, ctypes.c_float(1.0), kda.KDA_BF16, FAKE,
+                         kda.KDA_BF16] + [FAKE] * 5 + [FAKE, ws, None]
+
+    def call(**over):
+        a = list(args)
+        idx = {"q": 0, "B": 6, "dk": 9, "dv": 10, "d_o": 13, "gdt": 14, "dq": 15, "dbeta": 19,
+               "ws": 20, "ws_bytes": 21}
+        for k, v in over.items():
+            a[idx[k]] = v
+        return f(*a)
+
+    assert call(q=None) == -1
+    assert call(d_o=None) == -1
+    assert call(dbeta=None) == -1
+    assert call(dq=ODD) == -1
+    assert call(B=0) == -1
+    assert call(dk=96, dv=96) == -2
+    assert call(gdt=kda.KDA_BF16 + 7) == -1
+    assert call(ws=None) == -4
+    assert call(ws_bytes=ws - 1) == -4

@@ -38,9 +38,56 @@ namespace {
 constexpr int kTile = 8;                  // each thread holds an 8 x 8 block
 constexpr int kWin = 8;                   // tokens staged per window
 
-// workspace: the segment list (seg_start, seg_end, counters), then dq in fp32
-// [N, H, D], then the checkpoints S_{t-1} at chunk starts [ceil(N/64), H, D, D] fp32
-inline size_t bwd_list_bytes(int64_t N) { return (size_t(N) * 8 + 256 + 255) & ~size_t(255); }
+// workspace: the segment list (seg_start, seg_end, counters), the segments' order
+// (longest first), then dq in fp32 [N, H, D], then the checkpoints S_{t-1} at chunk starts
+// [ceil(N/64), H, D, D] fp32
+inline size_t bwd_list_bytes(int64_t N) { return (size_t(N) * 12 + 256 + 255) & ~size_t(255); }
+
+// Orders the segments longest first (a counting sort on 1024 buckets of log2 length,
+// 1/48 octave wide), so that the longest serial walks start at once rather than when
+// their turn in token order comes. One CTA of 1024 threads.
+constexpr int kOrderThreads = 1024;
+__global__ void __launch_bounds__(kOrderThreads, 1)
+order_segments_kernel(const int32_t* __restrict__ seg_start, const int32_t* __restrict__ seg_end,
+                      const int32_t* __restrict__ counters, int32_t* __restrict__ order) {
+    __shared__ int hist[kOrderThreads];
+    __shared__ int warp_sum[32];
+    const int n = counters[0];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    auto bucket = [&](int s) {          // 0 = longest
+        const float len = float(seg_end[s] - seg_start[s]);
+        const int b = int(__log2f(len) * 48.f);
+        return kOrderThreads - 1 - (b < kOrderThreads - 1 ? b : kOrderThreads - 1);
+    };
+    hist[tid] = 0;
+    __syncthreads();
+    for (int s = tid; s < n; s += kOrderThreads) atomicAdd(&hist[bucket(s)], 1);
+    __syncthreads();
+    // exclusive scan of hist, one bucket per thread
+    const int v = hist[tid];
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = warp_sum[lane];
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += x;
+        }
+        warp_sum[lane] = wi - w;
+    }
+    __syncthreads();
+    hist[tid] = warp_sum[warp] + incl - v;
+    __syncthreads();
+    for (int s = tid; s < n; s += kOrderThreads) order[atomicAdd(&hist[bucket(s)], 1)] = s;
+}
 
 template <int D> constexpr int bwd_threads() { return (D / kTile) * (D / kTile); }
 
@@ -99,8 +146,8 @@ __global__ void __launch_bounds__(bwd_threads<D>(), D == 64 ? 8 : 2)
 bwd_dq_kernel(const T* __restrict__ k, const T* __restrict__ v, const T* __restrict__ g,
               const T* __restrict__ beta, const T* __restrict__ d_o, int32_t H, float scale,
               const int32_t* __restrict__ seg_start, const int32_t* __restrict__ seg_end,
-              const int32_t* __restrict__ counters, To* __restrict__ dq,
-              float* __restrict__ dq32, float* __restrict__ ckpt) {
+              const int32_t* __restrict__ counters, const int32_t* __restrict__ order,
+              To* __restrict__ dq, float* __restrict__ dq32, float* __restrict__ ckpt) {
     constexpr int NG = D / kTile;
     constexpr int NT = NG * NG;
     extern __shared__ __align__(16) float smem[];
@@ -114,7 +161,7 @@ bwd_dq_kernel(const T* __restrict__ k, const T* __restrict__ v, const T* __restr
     const int rg = tid / NG, cg = tid % NG;
     const int64_t n_units = int64_t(counters[0]) * H;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const int64_t s_idx = u / H;
+        const int64_t s_idx = order[u / H];
         const int h = int(u % H);
         const int64_t p0 = seg_start[s_idx], p1 = seg_end[s_idx];
         float2 S[kTile][kTile / 2];
@@ -207,42 +254,49 @@ bwd_dq_kernel(const T* __restrict__ k, const T* __restrict__ v, const T* __restr
 }
 
 // ---- backward walk: dk, dv, dbeta, dg ------------------------------------------------------
+constexpr int kWinR = 16;                 // tokens staged per window of the backward walk
 template <int D> constexpr int dkv_smem_bytes() {
-    // staged q, do, k, v, exp(g), dq; out dk, dg, k u; per-warp dv partials; beta
-    return 9 * kWin * D * 4 + (bwd_threads<D>() / 32) * kWin * D * 4 + kWin * 4;
+    // staged q, do, k, v, exp(g), dq; out dk, dg, k u; per-warp dv partials; beta; the
+    // restart values of dg
+    return 9 * kWinR * D * 4 + (bwd_threads<D>() / 32) * kWinR * D * 4 + kWinR * 4 + D * 4;
 }
 
+// CTAs per SM of the backward walk: the full register file (no spills) for 128-wide heads
+template <int D> constexpr int dkv_ctas_per_sm() { return D == 64 ? 4 : 1; }
+
 template <typename T, typename To, int D>
-__global__ void __launch_bounds__(bwd_threads<D>(), D == 64 ? 4 : 2)
+__global__ void __launch_bounds__(bwd_threads<D>(), dkv_ctas_per_sm<D>())
 bwd_dkv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                const T* __restrict__ g, const T* __restrict__ beta, const T* __restrict__ d_o,
                const float* __restrict__ dq, const float* __restrict__ ckpt, int32_t H,
                float scale,
                const int32_t* __restrict__ seg_start, const int32_t* __restrict__ seg_end,
-               const int32_t* __restrict__ counters, To* __restrict__ dk, To* __restrict__ dv,
+               const int32_t* __restrict__ counters, const int32_t* __restrict__ order,
+               To* __restrict__ dk, To* __restrict__ dv,
                To* __restrict__ dg, To* __restrict__ dbeta) {
     constexpr int NG = D / kTile;
     constexpr int NT = NG * NG;
     constexpr int NW = NT / 32;
     extern __shared__ __align__(16) float smem[];
-    float* sq = smem;                     // [kWin][D]
-    float* sdo = sq + kWin * D;
-    float* sk = sdo + kWin * D;
-    float* sv = sk + kWin * D;
-    float* se = sv + kWin * D;
-    float* sdq = se + kWin * D;
-    float* sdk = sdq + kWin * D;          // outputs of the window
-    float* sdg = sdk + kWin * D;
-    float* sku = sdg + kWin * D;          // k_c u_c, summed into dbeta
-    float* part = sku + kWin * D;         // [NW][kWin][D] partial A^T k
-    float* sb = part + NW * kWin * D;     // [kWin] beta
+    float* sq = smem;                     // [kWinR][D]
+    float* sdo = sq + kWinR * D;
+    float* sk = sdo + kWinR * D;
+    float* sv = sk + kWinR * D;
+    float* se = sv + kWinR * D;
+    float* sdq = se + kWinR * D;
+    float* sdk = sdq + kWinR * D;          // outputs of the window
+    float* sdg = sdk + kWinR * D;
+    float* sku = sdg + kWinR * D;          // k_c u_c, summed into dbeta
+    float* part = sku + kWinR * D;         // [NW][kWinR][D] partial A^T k
+    float* sb = part + NW * kWinR * D;     // [kWinR] beta
+    float* sdir = sb + kWinR;              // [D] dg from its direct form at a chunk start
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int rg = tid / NG, cg = tid % NG;
     const int64_t n_units = int64_t(counters[0]) * H;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const int64_t s_idx = u / H;
+        const int64_t s_idx = order[u / H];
         const int h = int(u % H);
         const int64_t p0 = seg_start[s_idx], p1 = seg_end[s_idx];
         float2 X[kTile][kTile / 2];       // exp(g_{t+1}) * A_{t+1}: the carried adjoint
@@ -250,9 +304,9 @@ bwd_dkv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
         for (int i = 0; i < kTile; ++i)
 #pragma unroll
             for (int jp = 0; jp < kTile / 2; ++jp) X[i][jp] = make_float2(0.f, 0.f);
-        float run = 0.f;                  // lanes cg < 8: dg running sum of channel 8 rg + cg
+        float run = 0.f;                  // threads tid < D: dg running sum of channel tid
 
-        constexpr int PER = kWin * D / NT;
+        constexpr int PER = kWinR * D / NT;
         float rq[PER], rd[PER], rk[PER], rv[PER], rg_[PER], rdq[PER], rb[PER];
         // window [pw, pw + nw), the last window first
         auto load_window = [&](int64_t pw, int nw) {
@@ -272,7 +326,7 @@ bwd_dkv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
             }
         };
         int64_t hi = p1;
-        int64_t lo = (hi - p0 > kWin) ? hi - kWin : p0;
+        int64_t lo = (hi - p0 > kWinR) ? hi - kWinR : p0;
         load_window(lo, int(hi - lo));
         while (hi > p0) {
             const int nw = int(hi - lo);
@@ -291,7 +345,7 @@ bwd_dkv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
                 }
             }
             const int64_t nhi = lo;
-            const int64_t nlo = (nhi - p0 > kWin) ? nhi - kWin : p0;
+            const int64_t nlo = (nhi - p0 > kWinR) ? nhi - kWinR : p0;
             load_window(nlo, int(nhi - nlo));
             __syncthreads();
             for (int w = nw - 1; w >= 0; --w) {
@@ -354,7 +408,7 @@ bwd_dkv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
                         wk[jp].y += __shfl_xor_sync(0xffffffffu, wk[jp].y, m);
                     }
                 if (lane < NG) {                          // the warp's first row block
-                    float4* dst = reinterpret_cast<float4*>(part + (warp * kWin + w) * D + kTile * cg);
+                    float4* dst = reinterpret_cast<float4*>(part + (warp * kWinR + w) * D + kTile * cg);
                     dst[0] = make_float4(wk[0].x, wk[0].y, wk[1].x, wk[1].y);
                     dst[1] = make_float4(wk[2].x, wk[2].y, wk[3].x, wk[3].y);
                 }
@@ -363,12 +417,20 @@ bwd_dkv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
                     const float uc = pick8(uo, cg);
                     const float kc = pick8(ki, cg);
                     const float dkc = sb[w] * uc;
-                    run += pick8(qi, cg) * sdq[w * D + c] - kc * dkc;
-                    if (restart) run = pick8(direct, cg);
-                    if (pos == p0) run = 0.f;             // S_{t-1} = 0 at a segment's start
                     sdk[w * D + c] = dkc;
-                    sdg[w * D + c] = run;
+                    sdg[w * D + c] = pick8(qi, cg) * sdq[w * D + c] - kc * dkc;   // dL/dG_t
                     sku[w * D + c] = kc * uc;
+                    if (restart) sdir[c] = pick8(direct, cg);
+                }
+            }
+            __syncthreads();
+            if (tid < D) {                                // dg: the running sums, last token first
+                for (int w = nw - 1; w >= 0; --w) {
+                    const int64_t pos = lo + w;
+                    run += sdg[w * D + tid];
+                    if ((pos & (kChunk - 1)) == 0 && pos > p0) run = sdir[tid];
+                    if (pos == p0) run = 0.f;             // S_{t-1} = 0 at a segment's start
+                    sdg[w * D + tid] = run;
                 }
             }
             __syncthreads();
@@ -379,7 +441,7 @@ bwd_dkv_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __rest
                 dg[row * D + c] = from_f32<To>(sdg[e]);
                 float acc = 0.f;
 #pragma unroll
-                for (int wp = 0; wp < NW; ++wp) acc += part[(wp * kWin + w) * D + c];
+                for (int wp = 0; wp < NW; ++wp) acc += part[(wp * kWinR + w) * D + c];
                 dv[row * D + c] = from_f32<To>(sb[w] * acc);
             }
             for (int w = warp; w < nw; w += NW) {         // dbeta_t = sum_c k_c (A v)_c
@@ -404,9 +466,12 @@ kda_status_t launch_bwd_typed(const void* q, const void* k, const void* v, const
     const int32_t* seg_start = static_cast<const int32_t*>(ws);
     const int32_t* seg_end = seg_start + N;
     const int32_t* counters = seg_end + N;
+    int32_t* order = const_cast<int32_t*>(counters) + 64;
     float* dq32 = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + bwd_list_bytes(N));
     float* ckpt = dq32 + N * H * D;
     if (launch_segment_list(seg, B, T_len, ws, stream) != KDA_OK) return KDA_ERR_CUDA;
+    order_segments_kernel<<<1, kOrderThreads, 0, stream>>>(seg_start, seg_end, counters, order);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
     if (seg != nullptr) {
         zero_padding_grads<To><<<unsigned(N), 128, 0, stream>>>(
             seg, N, int64_t(H) * D, H, static_cast<To*>(dq), static_cast<To*>(dk),
@@ -422,12 +487,13 @@ kda_status_t launch_bwd_typed(const void* q, const void* k, const void* v, const
     bwd_dq_kernel<T, To, D><<<blocks, bwd_threads<D>(), dq_smem_bytes<D>(), stream>>>(
         static_cast<const T*>(k), static_cast<const T*>(v), static_cast<const T*>(g),
         static_cast<const T*>(beta), static_cast<const T*>(d_o), H, scale, seg_start, seg_end,
-        counters, static_cast<To*>(dq), dq32, ckpt);
+        counters, order, static_cast<To*>(dq), dq32, ckpt);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-    bwd_dkv_kernel<T, To, D><<<blocks, bwd_threads<D>(), dkv_smem_bytes<D>(), stream>>>(
+    const int dkv_blocks = max(1, sm_count()) * dkv_ctas_per_sm<D>();
+    bwd_dkv_kernel<T, To, D><<<dkv_blocks, bwd_threads<D>(), dkv_smem_bytes<D>(), stream>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
         static_cast<const T*>(g), static_cast<const T*>(beta), static_cast<const T*>(d_o),
-        dq32, ckpt, H, scale, seg_start, seg_end, counters, static_cast<To*>(dk),
+        dq32, ckpt, H, scale, seg_start, seg_end, counters, order, static_cast<To*>(dk),
         static_cast<To*>(dv), static_cast<To*>(dg), static_cast<To*>(dbeta));
     return launch_status();
 }

@@ -290,7 +290,8 @@ def run_gb300(args):
 
     def step(record=False):
         a = mark(record)
-        kda.kda_segids_to_cu_seqlens(seg, wl.max_segs, out=cu, n_segs_out=nseg)
+        if seg is not None:          # without ids every row is one segment: no scan
+            kda.kda_segids_to_cu_seqlens(seg, wl.max_segs, out=cu, n_segs_out=nseg)
         b = mark(record)
         for c, y in zip(convs, ys):
             kda.kda_short_conv_varlen(c.x, c.w, c.segment_ids, out=y)
@@ -311,7 +312,7 @@ def run_gb300(args):
         step(record=True)
     torch.cuda.synchronize()
     chunk_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_chunk)
-    seg_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_seg)
+    seg_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_seg) if seg is not None else None
     conv_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_conv) / len(convs)
     # the timed steps: one step captured in a CUDA graph (the same calls, on the
     # same buffers) and replayed K times
@@ -338,12 +339,12 @@ def run_gb300(args):
     clk = clocks.stop()
     ms_local = t0.elapsed_time(t1) / args.steps
     value, ms = job_throughput(N, ms_local, ws, dev)
-    real_tokens = int((seg != 0).sum().item())
+    real_tokens = int((seg != 0).sum().item()) if seg is not None else N
     if int(status.item()) != 0:
         print(f"warning: device status {int(status.item()):#x}", file=sys.stderr)
 
     # ---- per-segment state in and out (kda_chunk_fwd_varlen_state), timed apart ----
-    n_state = int(nseg.item())
+    n_state = int(nseg.item()) if seg is not None else wl.B
     st_gen = torch.Generator(device=dev).manual_seed(11)
     init = torch.randn(n_state, H, wl.d_qk, wl.d_v, device=dev, generator=st_gen) * 0.1
     state_ms = None
@@ -394,7 +395,7 @@ def run_gb300(args):
     # ---- e2e through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
-        host_in = {"seg": seg.cpu().pin_memory()}
+        host_in = {"seg": seg.cpu().pin_memory()} if seg is not None else {}
         for n in ("q", "k", "v", "g", "beta"):
             host_in[n] = getattr(kin, n).cpu().pin_memory()
         for i, c in enumerate(convs):
@@ -433,11 +434,13 @@ def run_gb300(args):
             if ev_out[b] is not None:
                 stream.wait_event(ev_out[b])
             d_in, d_out = dev_in[b], dev_out[b]
-            kda.kda_segids_to_cu_seqlens(d_in["seg"], wl.max_segs, out=cu, n_segs_out=nseg)
+            sd = d_in.get("seg")
+            if sd is not None:
+                kda.kda_segids_to_cu_seqlens(sd, wl.max_segs, out=cu, n_segs_out=nseg)
             for c in range(3):
-                kda.kda_short_conv_varlen(d_in[f"x{c}"], d_in[f"w{c}"], d_in["seg"], out=d_out[f"y{c}"])
+                kda.kda_short_conv_varlen(d_in[f"x{c}"], d_in[f"w{c}"], sd, out=d_out[f"y{c}"])
             kda.kda_chunk_fwd_varlen(d_in["q"], d_in["k"], d_in["v"], d_in["g"], d_in["beta"],
-                                     d_in["seg"], B=wl.B, T=wl.T, out=d_out["o"], workspace=work,
+                                     sd, B=wl.B, T=wl.T, out=d_out["o"], workspace=work,
                                      status=status)
             ev_comp[b] = torch.cuda.Event()
             ev_comp[b].record(stream)
@@ -488,7 +491,9 @@ def run_gb300(args):
         "data": "synthetic (seeded; Ling3-tiny packed shape, lognormal EOD-separated documents)",
         "config": {"workload": f"{wl.name} packed: B={wl.B} T={wl.T} H={H} D={wl.d_qk} bf16, "
                                f"max_segs={wl.max_segs}, conv width {wl.k_conv}",
-                   "step": "segids->cu_seqlens + 3 masked short convs + chunked KDA fwd",
+                   "step": ("segids->cu_seqlens + 3 masked short convs + chunked KDA fwd"
+                            if seg is not None else
+                            "3 causal short convs + chunked KDA fwd (segment_ids=None: no scan)"),
                    "timing": ("the step's calls captured once in a CUDA graph, replayed K times "
                               "between CUDA events; per-op times from an eager pass with events "
                               "between the calls"),
@@ -516,7 +521,7 @@ def run_gb300(args):
             if ms_ is not None
         },
         "real_tokens_per_s": real_tokens * ws / (ms / 1e3),
-        "gpu_launches": args.steps * 7,
+        "gpu_launches": args.steps * (7 if seg is not None else 6),
         "clocks": clk,
         "e2e": e2e,
     }

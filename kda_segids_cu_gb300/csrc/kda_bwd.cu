@@ -463,10 +463,10 @@ kda_status_t launch_bwd_typed(const void* q, const void* k, const void* v, const
                               int64_t T_len, int32_t H, float scale, void* dq, void* dk, void* dv,
                               void* dg, void* dbeta, void* ws, cudaStream_t stream) {
     const int64_t N = B * T_len;
-    const int32_t* seg_start = static_cast<const int32_t*>(ws);
-    const int32_t* seg_end = seg_start + N;
-    const int32_t* counters = seg_end + N;
-    int32_t* order = const_cast<int32_t*>(counters) + 64;
+    int32_t* seg_start = static_cast<int32_t*>(ws);
+    int32_t* seg_end = seg_start + N;
+    int32_t* counters = seg_end + N;
+    int32_t* order = counters + 64;
     float* dq32 = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + bwd_list_bytes(N));
     float* ckpt = dq32 + N * H * D;
     if (launch_segment_list(seg, B, T_len, ws, stream) != KDA_OK) return KDA_ERR_CUDA;

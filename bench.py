@@ -97,6 +97,13 @@ CHUNK_SOURCES = ("kda_segids_cu_gb300/csrc/kda_chunk_tc.cu", "kda_segids_cu_gb30
                  "kda_segids_cu_gb300/csrc/kda_plan.cuh")
 
 
+def workload_label(wl: synth.Workload) -> str:
+    """The workload as both arms name it in `config`."""
+    dt = "bf16" if wl.dtype == torch.bfloat16 else "fp32"
+    return (f"{wl.name} packed: B={wl.B} T={wl.T} H={wl.H} D={wl.d_qk} {dt}, "
+            f"max_segs={wl.max_segs}, conv width {wl.k_conv}")
+
+
 def chunk_traffic(wl: synth.Workload):
     import hashlib
     if wl.name != CHUNK_TRAFFIC["workload"]:
@@ -489,8 +496,7 @@ def run_gb300(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; Ling3-tiny packed shape, lognormal EOD-separated documents)",
-        "config": {"workload": f"{wl.name} packed: B={wl.B} T={wl.T} H={H} D={wl.d_qk} bf16, "
-                               f"max_segs={wl.max_segs}, conv width {wl.k_conv}",
+        "config": {"workload": workload_label(wl),
                    "step": ("segids->cu_seqlens + 3 masked short convs + chunked KDA fwd"
                             if seg is not None else
                             "3 causal short convs + chunked KDA fwd (segment_ids=None: no scan)"),
@@ -606,7 +612,7 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "impl": "reference",
-            "config": {"workload": f"{wl.name} packed: B={wl.B} T={wl.T} H={wl.H} D={wl.d_qk}",
+            "config": {"workload": workload_label(wl),
                        "step": "fp64 CPU oracle: cu_seqlens + 3 masked convs + recurrence"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt, "kind": "oracle",
                              "sample": sample},

@@ -63,3 +63,39 @@ def test_step_captured_in_a_graph_matches_eager():
         for name, a, b in zip(("cu_seqlens", "n_segs", "conv", "o", "o (state)", "final state"),
                               outs, eager):
             assert torch.equal(a, b), f"trial {trial}: graph replay differs from eager: {name}"
+
+
+def test_backward_captured_in_a_graph_matches_eager():
+    B, T, H, D = 2, 200, 2, 128
+    dev = torch.device("cuda")
+    first = _small_random(B, T, H, D, torch.bfloat16, seed=31, max_len=80, pad_prob=0.1)
+    seg = first.segment_ids.to(dev).contiguous()
+    q, k, v, g, beta = (t.to(dev).contiguous() for t in (first.q, first.k, first.v, first.g,
+                                                          first.beta))
+    d_o = torch.randn(q.shape, device=dev).bfloat16()
+    ws = torch.empty(int(kda.load_library().kda_chunk_bwd_varlen_workspace_size(
+        B, T, H, D, D, kda.KDA_BF16)), dtype=torch.uint8, device=dev)
+
+    def step():
+        return kda.kda_chunk_bwd_varlen(q, k, v, g, beta, d_o, seg, B=B, T=T, workspace=ws)
+
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        step()                                   # first call sets kernel attributes
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        outs = step()
+    torch.cuda.synchronize()
+    for trial in range(2):
+        new = _small_random(B, T, H, D, torch.bfloat16, seed=40 + trial, max_len=60, pad_prob=0.1)
+        for dst, src in ((seg, new.segment_ids), (q, new.q), (k, new.k), (v, new.v),
+                         (g, new.g), (beta, new.beta)):
+            _fill(dst, src)
+        d_o.copy_(torch.randn(q.shape, device=dev).bfloat16())
+        graph.replay()
+        torch.cuda.synchronize()
+        eager = step()
+        torch.cuda.synchronize()
+        for name, a, b in zip(("dq", "dk", "dv", "dg", "dbeta"), outs, eager):
+            assert torch.equal(a, b), f"trial {trial}: graph replay differs from eager: {name}"

@@ -237,3 +237,20 @@ def test_large_workloads_state_sampled_heads(name, heads):
     check_kda_output(o, ref, None if seg is None else seg.cpu(), wl.dtype, heads=heads,
                      label=name)
     _check_states(pick(fin), ref_fin, name)
+
+
+def test_tensor_core_state_segment_ids_none():
+    """bf16, 128-wide heads, segment_ids=None: row b is segment b. Equal bit for bit to
+    all-ones ids, and held to the oracle."""
+    B, T, H, D = 3, 200, 2, 128
+    inp = _small_random(B, T, H, D, torch.bfloat16, seed=21)
+    ones = torch.ones(B, T, dtype=torch.int32)
+    inp.segment_ids = ones
+    init = torch.randn(B, H, D, D, generator=torch.Generator().manual_seed(8)) * 0.3
+    o1, f1 = _run(inp, B, T, init, B, seg=ones)
+    on, fn = _run(inp, B, T, init, B, seg=None)
+    assert torch.equal(o1, on) and torch.equal(f1, fn)
+    ref, ref_fin = oracle.kda_fwd_state(inp.q, inp.k, inp.v, inp.g, inp.beta, None, B, T,
+                                        initial_state=init, n_state=B, want_final=True)
+    check_kda_output(on, ref, None, torch.bfloat16, label="None")
+    _check_states(fn, ref_fin, "None")

@@ -21,8 +21,9 @@
 //     the final state
 //         S_e = exp(G_e - G_{a-1}) * S_a + sum_{j=a..e} (beta_j k_j * exp(G_e - G_j)) v_j^T
 //     where the products with exp(...) scale the key rows.
-// The planner lists the chunks holding a start or the end of a carried segment; one CTA
-// takes one (listed chunk, head) at a time. fp32 arithmetic with exact exponentials (expf).
+// The planner lists the chunks holding a start or the end of a carried segment; each CTA
+// takes the next (listed chunk, head) from a work counter, so that units of unequal cost
+// spread evenly. fp32 arithmetic with exact exponentials (expf).
 #include "kda_common.cuh"
 #include "kda_plan.cuh"
 
@@ -283,7 +284,13 @@ state_tail_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     const int64_t slot_elems = int64_t(kTD) * kTD;
 
     const int64_t n_units = int64_t(pl.counters[3]) * H;
-    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+    __shared__ int s_unit;
+    for (;;) {
+        if (tid == 0) s_unit = atomicAdd(&pl.counters[4], 1);
+        __syncthreads();
+        const int64_t u = s_unit;
+        __syncthreads();                          // all have read it before it is rewritten
+        if (u >= n_units) break;
         const int64_t c = pl.active[u / H];
         const int h = int(u % H);
         const ChunkMeta m = pl.meta[c];

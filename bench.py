@@ -91,8 +91,8 @@ def chunk_flops_per_token_head(wl: synth.Workload) -> int:
 # `python bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline`. It holds only
 # for the kernel sources it was taken on (SHA-1 over the three files below);
 # after any change to them the bench reports null until a new capture.
-CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "1ca549941d4f7be20947b659ea696d4c8e32d321",
-                 "read": 557_721_600, "write": 117_912_320}
+CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "43757aaa09edad75df0f732515533ca47735632b",
+                 "read": 557_962_240, "write": 117_781_760}
 CHUNK_SOURCES = ("kda_segids_cu_gb300/csrc/kda_chunk_tc.cu", "kda_segids_cu_gb300/csrc/kda_sm100.cuh",
                  "kda_segids_cu_gb300/csrc/kda_plan.cuh")
 

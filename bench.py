@@ -92,7 +92,7 @@ def chunk_flops_per_token_head(wl: synth.Workload) -> int:
 # for the kernel sources it was taken on (SHA-1 over the three files below);
 # after any change to them the bench reports null until a new capture.
 CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "43757aaa09edad75df0f732515533ca47735632b",
-                 "read": 557_962_240, "write": 117_781_760}
+                 "read": 558_455_808, "write": 116_929_792}
 CHUNK_SOURCES = ("kda_segids_cu_gb300/csrc/kda_chunk_tc.cu", "kda_segids_cu_gb300/csrc/kda_sm100.cuh",
                  "kda_segids_cu_gb300/csrc/kda_plan.cuh")
 
@@ -282,6 +282,9 @@ def run_gb300(args):
     cu = torch.empty(wl.max_segs + 1, dtype=torch.int32, device=dev)
     nseg = torch.empty(1, dtype=torch.int32, device=dev)
     ys = [torch.empty_like(c.x) for c in convs]
+    # the convs produce q, k and v for the chunked forward ([B, T, H*D] read as [B*T, H, D]),
+    # as in the attention layer of [RFC-0025]; g and beta are inputs of their own
+    qkv = [y.view(N, H, wl.d_qk) for y in ys]
     o = torch.empty_like(kin.v)
     wsb = kda.chunk_fwd_workspace_bytes(wl.B, wl.T, H, wl.d_qk, wl.d_v, wl.dtype)
     work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
@@ -303,7 +306,7 @@ def run_gb300(args):
         for c, y in zip(convs, ys):
             kda.kda_short_conv_varlen(c.x, c.w, c.segment_ids, out=y)
         e0 = mark(record)
-        kda.kda_chunk_fwd_varlen(kin.q, kin.k, kin.v, kin.g, kin.beta, seg, B=wl.B, T=wl.T,
+        kda.kda_chunk_fwd_varlen(qkv[0], qkv[1], qkv[2], kin.g, kin.beta, seg, B=wl.B, T=wl.T,
                                  out=o, workspace=work, status=status)
         e1 = mark(record)
         if record:
@@ -402,15 +405,15 @@ def run_gb300(args):
     # ---- e2e through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
+        # the step's inputs come from pinned host memory; its result, o, goes back. The conv
+        # outputs (q, k, v) stay on the device, as intermediates of the step.
         host_in = {"seg": seg.cpu().pin_memory()} if seg is not None else {}
-        for n in ("q", "k", "v", "g", "beta"):
+        for n in ("g", "beta"):
             host_in[n] = getattr(kin, n).cpu().pin_memory()
         for i, c in enumerate(convs):
             host_in[f"x{i}"] = c.x.cpu().pin_memory()
             host_in[f"w{i}"] = c.w.cpu().pin_memory()
         host_out = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory()}
-        for i in range(3):
-            host_out[f"y{i}"] = torch.empty(ys[i].shape, dtype=ys[i].dtype).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in host_in.values())
         d2h = sum(v.numel() * v.element_size() for v in host_out.values())
         # Steps are pipelined: two copy streams bring step i's inputs in while the
@@ -420,6 +423,7 @@ def run_gb300(args):
         dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(nb)]
         dev_out = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in host_out.items()}
                    for _ in range(nb)]
+        dev_mid = [[torch.empty_like(y) for y in ys] for _ in range(nb)]
         s_in = [torch.cuda.Stream(device=dev) for _ in range(2)]
         s_out = torch.cuda.Stream(device=dev)
         keys = sorted(host_in, key=lambda k: -host_in[k].numel() * host_in[k].element_size())
@@ -444,11 +448,12 @@ def run_gb300(args):
             sd = d_in.get("seg")
             if sd is not None:
                 kda.kda_segids_to_cu_seqlens(sd, wl.max_segs, out=cu, n_segs_out=nseg)
+            mid = dev_mid[b]
             for c in range(3):
-                kda.kda_short_conv_varlen(d_in[f"x{c}"], d_in[f"w{c}"], sd, out=d_out[f"y{c}"])
-            kda.kda_chunk_fwd_varlen(d_in["q"], d_in["k"], d_in["v"], d_in["g"], d_in["beta"],
-                                     sd, B=wl.B, T=wl.T, out=d_out["o"], workspace=work,
-                                     status=status)
+                kda.kda_short_conv_varlen(d_in[f"x{c}"], d_in[f"w{c}"], sd, out=mid[c])
+            kda.kda_chunk_fwd_varlen(*[y.view(N, H, wl.d_qk) for y in mid], d_in["g"],
+                                     d_in["beta"], sd, B=wl.B, T=wl.T, out=d_out["o"],
+                                     workspace=work, status=status)
             ev_comp[b] = torch.cuda.Event()
             ev_comp[b].record(stream)
             s_out.wait_event(ev_comp[b])
@@ -497,13 +502,18 @@ def run_gb300(args):
         "dtype": "bf16",
         "data": "synthetic (seeded; Ling3-tiny packed shape, lognormal EOD-separated documents)",
         "config": {"workload": workload_label(wl),
-                   "step": ("segids->cu_seqlens + 3 masked short convs + chunked KDA fwd"
-                            if seg is not None else
-                            "3 causal short convs + chunked KDA fwd (segment_ids=None: no scan)"),
+                   "step": ("segids->cu_seqlens + 3 masked short convs (producing q, k, v) + "
+                            "chunked KDA fwd" if seg is not None else
+                            "3 causal short convs (producing q, k, v) + chunked KDA fwd "
+                            "(segment_ids=None: no scan)"),
                    "timing": ("the step's calls captured once in a CUDA graph, replayed K times "
                               "between CUDA events; per-op times from an eager pass with events "
                               "between the calls"),
-                   "l2": "inputs larger than L2 (chunk inputs 537 MB, conv inputs 403 MB)",
+                   "l2": (f"inputs larger than L2 (conv inputs "
+                          f"{sum(c.x.numel() * c.x.element_size() for c in convs) / 1e6:.0f} MB, "
+                          f"g and beta "
+                          f"{(kin.g.numel() + kin.beta.numel()) * kin.g.element_size() / 1e6:.0f}"
+                          f" MB)"),
                    "parallelism": f"replicas x{ws} (rows independent)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": chunk_traffic(wl),

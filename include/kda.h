@@ -26,8 +26,8 @@
  *   - Sizes: B*T < 2^31.
  *   - Every call can be captured in a CUDA graph: it makes no host round trip,
  *     allocates nothing and launches only on `stream`. Make one call of each
- *     entry point (per kernel variant) before capturing, since the first call
- *     sets kernel attributes.
+ *     entry point (per kernel variant) on a device before capturing there,
+ *     since the first call on each device sets kernel attributes.
  */
 #ifndef KDA_H_
 #define KDA_H_

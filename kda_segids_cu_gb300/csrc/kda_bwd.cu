@@ -478,11 +478,9 @@ kda_status_t launch_bwd_typed(const void* q, const void* k, const void* v, const
             static_cast<To*>(dv), static_cast<To*>(dg), static_cast<To*>(dbeta));
         if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
     }
-    static const cudaError_t a1 = cudaFuncSetAttribute(
-        bwd_dq_kernel<T, To, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem_bytes<D>());
-    static const cudaError_t a2 = cudaFuncSetAttribute(
-        bwd_dkv_kernel<T, To, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv_smem_bytes<D>());
-    if (a1 != cudaSuccess || a2 != cudaSuccess) return KDA_ERR_CUDA;
+    if (dynamic_smem_attr<bwd_dq_kernel<T, To, D>>(dq_smem_bytes<D>()) != cudaSuccess ||
+        dynamic_smem_attr<bwd_dkv_kernel<T, To, D>>(dkv_smem_bytes<D>()) != cudaSuccess)
+        return KDA_ERR_CUDA;
     const int blocks = max(1, sm_count()) * (D == 64 ? 8 : 2);
     bwd_dq_kernel<T, To, D><<<blocks, bwd_threads<D>(), dq_smem_bytes<D>(), stream>>>(
         static_cast<const T*>(k), static_cast<const T*>(v), static_cast<const T*>(g),

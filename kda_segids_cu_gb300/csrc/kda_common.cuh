@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "kda.h"
 
 namespace kda {
@@ -17,6 +19,22 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 
 inline kda_status_t launch_status() {
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+// Raises kernel `Func`'s dynamic shared-memory limit to `bytes` on the current device, once
+// per device (the attribute belongs to the device; a process may drive several).
+constexpr int kMaxDevices = 64;
+template <auto Func>
+cudaError_t dynamic_smem_attr(int bytes) {
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t err[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [dev, bytes] {
+        err[dev] = cudaFuncSetAttribute(Func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    });
+    return err[dev];
 }
 
 inline int sm_count() {

@@ -246,10 +246,8 @@ kda_status_t launch_typed(const void* x, const void* w, const int32_t* seg, void
     switch (K) {
 #define KDA_CONV_CASE(KK)                                                                      \
     case KK: {                                                                                 \
-        static cudaError_t attr = cudaFuncSetAttribute(                                        \
-            short_conv_kernel<T, KK>, cudaFuncAttributeMaxDynamicSharedMemorySize,              \
-            conv_smem_bytes());                                                                \
-        if (attr != cudaSuccess) return KDA_ERR_CUDA;                                          \
+        if (dynamic_smem_attr<short_conv_kernel<T, KK>>(conv_smem_bytes()) != cudaSuccess)     \
+            return KDA_ERR_CUDA;                                                               \
         short_conv_kernel<T, KK><<<grid, kConvThreads, conv_smem_bytes(), stream>>>(           \
             xp, wp, seg, yp, T_len, F, span, spans);                                           \
         break;                                                                                 \

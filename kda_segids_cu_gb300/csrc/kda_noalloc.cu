@@ -19,7 +19,7 @@ namespace {
 // address: the device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
+using kda::kMaxDevices;
 std::once_flag g_once[kMaxDevices];
 void* g_addr[kMaxDevices];
 cudaError_t g_err[kMaxDevices];

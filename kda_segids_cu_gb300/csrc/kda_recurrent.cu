@@ -330,17 +330,13 @@ static kda_status_t launch_recurrent_typed(const void* q, const void* k, const v
     const T* bp = static_cast<const T*>(beta);
     To* op = static_cast<To*>(o);
     if (D == 64) {
-        static const cudaError_t attr = cudaFuncSetAttribute(
-            recurrent_kernel<T, To, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-            rec_smem_bytes<64>());
-        if (attr != cudaSuccess) return KDA_ERR_CUDA;
+        if (dynamic_smem_attr<recurrent_kernel<T, To, 64>>(rec_smem_bytes<64>()) != cudaSuccess)
+            return KDA_ERR_CUDA;
         recurrent_kernel<T, To, 64><<<blocks, rec_threads<64>(), rec_smem_bytes<64>(), stream>>>(
             qp, kp, vp, gp, bp, H, scale, seg_start, seg_end, counters, op, init, fin, n_state);
     } else {
-        static const cudaError_t attr = cudaFuncSetAttribute(
-            recurrent_kernel<T, To, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-            rec_smem_bytes<128>());
-        if (attr != cudaSuccess) return KDA_ERR_CUDA;
+        if (dynamic_smem_attr<recurrent_kernel<T, To, 128>>(rec_smem_bytes<128>()) != cudaSuccess)
+            return KDA_ERR_CUDA;
         recurrent_kernel<T, To, 128><<<blocks, rec_threads<128>(), rec_smem_bytes<128>(),
                                        stream>>>(qp, kp, vp, gp, bp, H, scale, seg_start, seg_end,
                                                  counters, op, init, fin, n_state);

@@ -392,9 +392,8 @@ kda_status_t launch_tail_typed(const void* q, const void* k, const void* v, cons
                                const void* beta, int64_t N, int32_t H, float scale, void* o,
                                void* ws, const float* init, float* fin, int64_t n_state,
                                cudaStream_t stream) {
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        state_tail_kernel<To>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTailSmem));
-    if (attr != cudaSuccess) return KDA_ERR_CUDA;
+    if (dynamic_smem_attr<state_tail_kernel<To>>(int(kTailSmem)) != cudaSuccess)
+        return KDA_ERR_CUDA;
     const int blocks = max(1, sm_count());
     state_tail_kernel<To><<<blocks, kTailThreads, kTailSmem, stream>>>(
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),

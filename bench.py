@@ -91,8 +91,8 @@ def chunk_flops_per_token_head(wl: synth.Workload) -> int:
 # `python bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline`. It holds only
 # for the kernel sources it was taken on (SHA-1 over the three files below);
 # after any change to them the bench reports null until a new capture.
-CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "44ee8ec1af0325a33536fdf71e4147c4dd02eb93",
-                 "read": 558_692_608, "write": 117_225_472}
+CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "bd37f7cc318680d5ce82a8c015bc545f2b04fe4f",
+                 "read": 558_399_232, "write": 116_986_624}
 CHUNK_SOURCES = ("kda_segids_cu_gb300/csrc/kda_chunk_tc.cu", "kda_segids_cu_gb300/csrc/kda_sm100.cuh",
                  "kda_segids_cu_gb300/csrc/kda_plan.cuh")
 

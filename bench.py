@@ -324,11 +324,32 @@ def run_gb300(args):
     chunk_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_chunk)
     seg_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_seg) if seg is not None else None
     conv_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_conv) / len(convs)
-    # the timed steps: one step captured in a CUDA graph (the same calls, on the
-    # same buffers) and replayed K times
+    # the timed steps: one step captured in a CUDA graph (the same calls, on the same
+    # buffers) and replayed K times. The calls that read only the segment ids (the
+    # cu_seqlens scan and the chunk plan) run on a side stream of the graph, concurrent with
+    # the convs; the forward joins it and takes the plan from the workspace.
+    side = torch.cuda.Stream(device=dev)
+
+    def graph_step():
+        cur = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(cur)
+        side.wait_event(fork)
+        with torch.cuda.stream(side):
+            if seg is not None:
+                kda.kda_segids_to_cu_seqlens(seg, wl.max_segs, out=cu, n_segs_out=nseg)
+            kda.kda_chunk_plan_varlen(seg, wl.B, wl.T, H, wl.d_qk, wl.d_v, wl.dtype, work)
+        join = torch.cuda.Event()
+        join.record(side)
+        for c, y in zip(convs, ys):
+            kda.kda_short_conv_varlen(c.x, c.w, c.segment_ids, out=y)
+        cur.wait_event(join)
+        kda.kda_chunk_fwd_varlen(qkv[0], qkv[1], qkv[2], kin.g, kin.beta, seg, B=wl.B, T=wl.T,
+                                 out=o, workspace=work, status=status, planned=True)
+
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        step()
+        graph_step()
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
@@ -507,8 +528,9 @@ def run_gb300(args):
                             "3 causal short convs (producing q, k, v) + chunked KDA fwd "
                             "(segment_ids=None: no scan)"),
                    "timing": ("the step's calls captured once in a CUDA graph, replayed K times "
-                              "between CUDA events; per-op times from an eager pass with events "
-                              "between the calls"),
+                              "between CUDA events (the scan and the chunk plan on a side stream "
+                              "of the graph, beside the convs); per-op times from an eager pass "
+                              "of the plain calls with events between them"),
                    "l2": (f"inputs larger than L2 (conv inputs "
                           f"{sum(c.x.numel() * c.x.element_size() for c in convs) / 1e6:.0f} MB, "
                           f"g and beta "

@@ -160,6 +160,47 @@ kda_status_t kda_chunk_fwd_varlen(const void *q, const void *k, const void *v, c
                                   kda_stream_t stream);
 
 /*
+ * kda_chunk_plan_varlen / kda_chunk_fwd_varlen_planned -- kda_chunk_fwd_varlen
+ * in two calls. The plan (where segments start in each 64-token chunk, and the
+ * chunk ranges that the kernel's CTAs take in turn) depends only on
+ * segment_ids and the sizes. So a caller may compute it on another stream
+ * while the kernels that produce q, k, v and g run, and join before the
+ * forward. kda_chunk_plan_varlen(segment_ids, B, T, H, d_qk, d_v, dtype, ws)
+ * followed by kda_chunk_fwd_varlen_planned(..., ws, ...) with the same
+ * segment_ids contents and sizes gives kda_chunk_fwd_varlen's result bit for
+ * bit.
+ *
+ *   kda_chunk_plan_varlen    writes the plan into `workspace` (the forward's
+ *                            workspace: same size rule, alignment and
+ *                            argument checks). It reads segment_ids only.
+ *   kda_chunk_fwd_varlen_planned
+ *                            takes kda_chunk_fwd_varlen's arguments. Its
+ *                            workspace must hold a plan of the same
+ *                            segment_ids contents, B, T, H, d_qk, d_v and
+ *                            dtype, complete or ordered before the call
+ *                            (same stream, or an event). A plan serves any
+ *                            number of planned calls, one at a time, until
+ *                            another call writes the workspace.
+ *
+ * Paths that plan inside the forward (dtype KDA_F32, or 64-wide heads) have
+ * nothing to plan ahead: kda_chunk_plan_varlen only checks its arguments and
+ * the planned call plans for itself. A planned call on a workspace without a
+ * matching plan is undefined (wrong or missing outputs). Returns as
+ * kda_chunk_fwd_varlen.
+ */
+kda_status_t kda_chunk_plan_varlen(const int32_t *segment_ids, int64_t B, int64_t T, int32_t H,
+                                   int32_t d_qk, int32_t d_v, kda_dtype_t dtype, void *workspace,
+                                   size_t workspace_bytes, kda_stream_t stream);
+
+kda_status_t kda_chunk_fwd_varlen_planned(const void *q, const void *k, const void *v,
+                                          const void *g, const void *beta,
+                                          const int32_t *segment_ids, int64_t B, int64_t T,
+                                          int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                          kda_dtype_t dtype, kda_dtype_t out_dtype, void *o,
+                                          void *workspace, size_t workspace_bytes,
+                                          uint32_t *status_dev, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_varlen_state -- kda_chunk_fwd_varlen with per-segment recurrent
  * state in and out: the initial_state and output_final_state kwargs that
  * [RFC-0026] passes to the chunked KDA call, one state per packed sequence.

@@ -61,6 +61,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                          ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, vp,
                                          ctypes.c_size_t, u32p, vp]
     lib.kda_chunk_fwd_varlen.restype = ctypes.c_int
+    lib.kda_chunk_plan_varlen.argtypes = [vp, i64, i64, i32, i32, i32, ctypes.c_int, vp,
+                                          ctypes.c_size_t, vp]
+    lib.kda_chunk_plan_varlen.restype = ctypes.c_int
+    lib.kda_chunk_fwd_varlen_planned.argtypes = lib.kda_chunk_fwd_varlen.argtypes
+    lib.kda_chunk_fwd_varlen_planned.restype = ctypes.c_int
     lib.kda_chunk_fwd_varlen_state.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32,
                                                ctypes.c_float, ctypes.c_int, ctypes.c_int, vp,
                                                vp, vp, i64, vp, ctypes.c_size_t, u32p, vp]
@@ -212,19 +217,43 @@ def kda_chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: t
                          stream=None, out: torch.Tensor | None = None,
                          workspace: torch.Tensor | None = None,
                          status: torch.Tensor | None = None,
-                         out_dtype: torch.dtype | None = None) -> torch.Tensor:
+                         out_dtype: torch.dtype | None = None,
+                         planned: bool = False) -> torch.Tensor:
     """Packed KDA forward. q, k, g: [B, T, H, Dk], [1, B*T, H, Dk] or [B*T, H, Dk];
     v like q with Dv; beta [..., H]; segment_ids int32 [B, T] or None.
     Returns o shaped like v, of `out_dtype` (default: the input dtype; float32
-    is also accepted)."""
+    is also accepted). planned=True skips the planning: `workspace` must hold the
+    plan of these segment ids and sizes from kda_chunk_plan_varlen."""
+    if planned and workspace is None:
+        raise ValueError("planned=True needs the workspace that holds the plan")
     q, k, v, g, beta, seg, B, T, H, Dk, Dv, dt, odt, o, workspace = _chunk_args(
         q, k, v, g, beta, segment_ids, B, T, out, workspace, out_dtype)
-    _check("kda_chunk_fwd_varlen",
-           load_library().kda_chunk_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                                               _ptr(seg), B, T, H, Dk, Dv, float(scale), dt,
-                                               odt, _ptr(o), _ptr(workspace), workspace.numel(),
-                                               _ptr(status), _stream_ptr(stream)))
+    lib = load_library()
+    fn, name = ((lib.kda_chunk_fwd_varlen_planned, "kda_chunk_fwd_varlen_planned") if planned
+                else (lib.kda_chunk_fwd_varlen, "kda_chunk_fwd_varlen"))
+    _check(name, fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(seg), B, T, H, Dk, Dv,
+                    float(scale), dt, odt, _ptr(o), _ptr(workspace), workspace.numel(),
+                    _ptr(status), _stream_ptr(stream)))
     return o
+
+
+def kda_chunk_plan_varlen(segment_ids: torch.Tensor | None, B: int, T: int, H: int, d_qk: int,
+                          d_v: int, dtype: torch.dtype, workspace: torch.Tensor,
+                          stream=None) -> torch.Tensor:
+    """Writes the plan of a forward over these segment ids and sizes into `workspace`
+    (the forward's workspace), for kda_chunk_fwd_varlen(..., planned=True). Reads only
+    segment_ids; returns the workspace."""
+    seg = None
+    if segment_ids is not None:
+        seg = _dev(segment_ids, "segment_ids")
+        if seg.dtype != torch.int32 or tuple(seg.shape) != (B, T):
+            raise ValueError("segment_ids must be int32 [B, T]")
+    ws = _dev(workspace, "workspace")
+    _check("kda_chunk_plan_varlen",
+           load_library().kda_chunk_plan_varlen(_ptr(seg), B, T, H, d_qk, d_v,
+                                                _dtype_code(dtype), _ptr(ws), ws.numel(),
+                                                _stream_ptr(stream)))
+    return ws
 
 
 def kda_chunk_fwd_varlen_state(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
@@ -313,6 +342,6 @@ def kda_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tenso
 
 
 __all__ = ["kda_segids_to_cu_seqlens", "kda_short_conv_varlen", "kda_chunk_fwd_varlen",
-           "kda_chunk_fwd_varlen_state", "kda_chunk_bwd_varlen", "kda_varlen",
+           "kda_chunk_plan_varlen", "kda_chunk_fwd_varlen_state", "kda_chunk_bwd_varlen", "kda_varlen",
            "chunk_fwd_workspace_bytes", "load_library", "header_functions", "KdaError",
            "KDA_DEV_DECAY_RANGE"]

@@ -14,11 +14,13 @@ kda_status_t launch_recurrent_state(const void* q, const void* k, const void* v,
                                     int32_t H, int32_t D, float scale, kda_dtype_t dtype,
                                     kda_dtype_t out_dtype, void* o, void* ws, const float* init,
                                     float* fin, int64_t n_state, cudaStream_t stream);
+kda_status_t launch_chunk_plan(const int32_t* seg, int64_t B, int64_t T, int32_t H, int32_t D,
+                               bool with_state, void* ws, cudaStream_t stream);
 kda_status_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* g,
                              const void* beta, const int32_t* seg, int64_t B, int64_t T,
                              int32_t H, int32_t D, float scale, kda_dtype_t out_dtype, void* o,
                              void* ws, uint32_t* status_dev, const float* init, float* fin,
-                             int64_t n_state, cudaStream_t stream);
+                             int64_t n_state, bool plan, cudaStream_t stream);
 size_t bwd_workspace_bytes(int64_t N, int32_t H, int32_t D);
 kda_status_t launch_bwd(const void* q, const void* k, const void* v, const void* g,
                         const void* beta, const void* d_o, const int32_t* seg, int64_t B,
@@ -90,12 +92,14 @@ size_t kda_chunk_fwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int3
     return tc > rec ? tc : rec;
 }
 
-kda_status_t kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, const void* g,
-                                  const void* beta, const int32_t* segment_ids, int64_t B,
-                                  int64_t T, int32_t H, int32_t d_qk, int32_t d_v, float scale,
-                                  kda_dtype_t dtype, kda_dtype_t out_dtype, void* o,
-                                  void* workspace, size_t workspace_bytes,
-                                  uint32_t* status_dev, kda_stream_t stream) {
+namespace {
+
+// The checks kda_chunk_fwd_varlen and kda_chunk_fwd_varlen_planned share.
+kda_status_t check_fwd_args(const void* q, const void* k, const void* v, const void* g,
+                            const void* beta, const int32_t* segment_ids, int64_t B, int64_t T,
+                            int32_t H, int32_t d_qk, int32_t d_v, kda_dtype_t dtype,
+                            kda_dtype_t out_dtype, const void* o, const void* workspace,
+                            size_t workspace_bytes, const uint32_t* status_dev) {
     if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
     if (!valid_dtype(dtype) || !valid_dtype(out_dtype) || !token_count_ok(B, T) || H < 1 ||
         d_qk < 1 || d_v < 1)
@@ -111,12 +115,64 @@ kda_status_t kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, c
     const size_t need = kda_chunk_fwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
     if (!workspace || workspace_bytes < need || !kda::aligned(workspace, 256))
         return KDA_ERR_WORKSPACE;
+    return KDA_OK;
+}
+
+kda_status_t chunk_fwd(const void* q, const void* k, const void* v, const void* g,
+                       const void* beta, const int32_t* segment_ids, int64_t B, int64_t T,
+                       int32_t H, int32_t d_qk, int32_t d_v, float scale, kda_dtype_t dtype,
+                       kda_dtype_t out_dtype, void* o, void* workspace, size_t workspace_bytes,
+                       uint32_t* status_dev, bool plan, kda_stream_t stream) {
+    const kda_status_t chk = check_fwd_args(q, k, v, g, beta, segment_ids, B, T, H, d_qk, d_v,
+                                            dtype, out_dtype, o, workspace, workspace_bytes,
+                                            status_dev);
+    if (chk != KDA_OK) return chk;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == KDA_BF16)
         return kda::launch_chunk_tc(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale,
-                                    out_dtype, o, workspace, status_dev, nullptr, nullptr, 0, st);
+                                    out_dtype, o, workspace, status_dev, nullptr, nullptr, 0,
+                                    plan, st);
     return kda::launch_recurrent(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale, dtype,
                                  out_dtype, o, workspace, st);
+}
+
+}  // namespace
+
+kda_status_t kda_chunk_fwd_varlen(const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const int32_t* segment_ids, int64_t B,
+                                  int64_t T, int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                  kda_dtype_t dtype, kda_dtype_t out_dtype, void* o,
+                                  void* workspace, size_t workspace_bytes,
+                                  uint32_t* status_dev, kda_stream_t stream) {
+    return chunk_fwd(q, k, v, g, beta, segment_ids, B, T, H, d_qk, d_v, scale, dtype, out_dtype,
+                     o, workspace, workspace_bytes, status_dev, true, stream);
+}
+
+kda_status_t kda_chunk_plan_varlen(const int32_t* segment_ids, int64_t B, int64_t T, int32_t H,
+                                   int32_t d_qk, int32_t d_v, kda_dtype_t dtype, void* workspace,
+                                   size_t workspace_bytes, kda_stream_t stream) {
+    if (!valid_dtype(dtype) || !token_count_ok(B, T) || H < 1 || d_qk < 1 || d_v < 1)
+        return KDA_ERR_INVALID_ARG;
+    if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return KDA_ERR_UNSUPPORTED;
+    if (int64_t(H) * d_qk > 65536) return KDA_ERR_UNSUPPORTED;
+    if (segment_ids && !kda::aligned(segment_ids, 4)) return KDA_ERR_INVALID_ARG;
+    const size_t need = kda_chunk_fwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
+    if (!workspace || workspace_bytes < need || !kda::aligned(workspace, 256))
+        return KDA_ERR_WORKSPACE;
+    if (dtype != KDA_BF16) return KDA_OK;     // the fp32 path plans inside its call
+    return kda::launch_chunk_plan(segment_ids, B, T, H, d_qk, false, workspace,
+                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+kda_status_t kda_chunk_fwd_varlen_planned(const void* q, const void* k, const void* v,
+                                          const void* g, const void* beta,
+                                          const int32_t* segment_ids, int64_t B, int64_t T,
+                                          int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                          kda_dtype_t dtype, kda_dtype_t out_dtype, void* o,
+                                          void* workspace, size_t workspace_bytes,
+                                          uint32_t* status_dev, kda_stream_t stream) {
+    return chunk_fwd(q, k, v, g, beta, segment_ids, B, T, H, d_qk, d_v, scale, dtype, out_dtype,
+                     o, workspace, workspace_bytes, status_dev, false, stream);
 }
 
 kda_status_t kda_chunk_fwd_varlen_state(const void* q, const void* k, const void* v,
@@ -150,7 +206,7 @@ kda_status_t kda_chunk_fwd_varlen_state(const void* q, const void* k, const void
     if (dtype == KDA_BF16 && d_qk == 128)   // tensor-core chunked form, then the state pass
         return kda::launch_chunk_tc(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale,
                                     out_dtype, o, workspace, status_dev, initial_state,
-                                    final_state, n_state, st);
+                                    final_state, n_state, true, st);
     return kda::launch_recurrent_state(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale, dtype,
                                        out_dtype, o, workspace, initial_state, final_state,
                                        n_state, st);

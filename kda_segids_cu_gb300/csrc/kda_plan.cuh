@@ -14,7 +14,8 @@ struct ChunkMeta {
 
 struct Plan {                      // device view of the workspace
     int32_t* counters;             // [0] n_units, [1] next item, [2] n_chunks, [3] n_active,
-                                   // [4] next unit of the state pass
+                                   // [4] next unit of the state pass, [5] chunk-kernel CTAs
+                                   // finished (the last one rewinds [1] and [5])
     ChunkMeta* meta;               // [n_chunks]
     int32_t* first_cut;            // [n_chunks] first start-or-padding row, 64 if none
     int32_t* block_cut;            // [n_blocks]

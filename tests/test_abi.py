@@ -61,8 +61,9 @@ def test_conv_rejects_invalid_arguments(lib):
     assert f(FAKE, FAKE, None, FAKE, 1, 4, 8, 4, 3, None) == -1     # dtype
 
 
-def test_chunk_rejects_invalid_arguments(lib):
-    f = lib.kda_chunk_fwd_varlen
+@pytest.mark.parametrize("fname", ["kda_chunk_fwd_varlen", "kda_chunk_fwd_varlen_planned"])
+def test_chunk_rejects_invalid_arguments(lib, fname):
+    f = getattr(lib, fname)
     ws = lib.kda_chunk_fwd_varlen_workspace_size(1, 64, 2, 64, 64, kda.KDA_BF16)
     args = [FAKE] * 5 + [None, 1, 64, 2, 64, 64, ctypes.c_float(1.0), kda.KDA_BF16, kda.KDA_BF16,
                          FAKE, FAKE, ws, None, None]
@@ -88,6 +89,31 @@ def test_chunk_rejects_invalid_arguments(lib):
     assert call(ws_bytes=ws - 1) == -4
     assert call(ws=ctypes.c_void_p(4096 + 16)) == -4          # workspace must be 256-aligned
     assert call(status=ODD) == -1
+
+
+def test_chunk_plan_rejects_invalid_arguments(lib):
+    f = lib.kda_chunk_plan_varlen
+    ws = lib.kda_chunk_fwd_varlen_workspace_size(1, 64, 2, 128, 128, kda.KDA_BF16)
+    args = [FAKE, 1, 64, 2, 128, 128, kda.KDA_BF16, FAKE, ws, None]
+
+    def call(**over):
+        a = list(args)
+        idx = {"seg": 0, "B": 1, "T": 2, "H": 3, "dk": 4, "dv": 5, "dtype": 6, "ws": 7,
+               "ws_bytes": 8}
+        for k, v in over.items():
+            a[idx[k]] = v
+        return f(*a)
+
+    assert call(seg=ODD) == -1
+    assert call(B=0) == -1
+    assert call(T=0) == -1
+    assert call(H=0) == -1
+    assert call(dtype=5) == -1
+    assert call(dk=96, dv=96) == -2
+    assert call(dk=64, dv=128) == -2
+    assert call(ws=None) == -4
+    assert call(ws_bytes=ws - 1) == -4
+    assert call(ws=ctypes.c_void_p(4096 + 16)) == -4
 
 
 def test_chunk_state_rejects_invalid_arguments(lib):

@@ -167,6 +167,36 @@ def test_packed_equals_per_document():
     check_kda_output(packed, alone.double(), inp.segment_ids, wl.dtype, label="packed vs alone")
 
 
+@pytest.mark.parametrize("dtype,D", [(torch.bfloat16, 128), (torch.bfloat16, 64),
+                                     (torch.float32, 64)])
+def test_planned_calls_match_plain_call(dtype, D):
+    """A plan made on another stream, then planned forwards on it (the second reuses the
+    plan: the kernel rewinds its work counter), give the plain call's output bit for bit."""
+    B, T, H = 2, 700, 3
+    inp = _small_random(B, T, H, D, dtype, seed=31, max_len=150, pad_prob=0.05)
+    q, k, v, g, beta = (t.cuda().contiguous() for t in (inp.q, inp.k, inp.v, inp.g, inp.beta))
+    seg = inp.segment_ids.cuda().contiguous()
+    plain = kda.kda_chunk_fwd_varlen(q, k, v, g, beta, seg, B=B, T=T)
+    ws = torch.empty(max(kda.chunk_fwd_workspace_bytes(B, T, H, D, D, dtype), 256),
+                     dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        kda.kda_chunk_plan_varlen(seg, B, T, H, D, D, dtype, ws)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        o = kda.kda_chunk_fwd_varlen(q, k, v, g, beta, seg, B=B, T=T, workspace=ws,
+                                     planned=True)
+        torch.cuda.synchronize()
+        assert torch.equal(o, plain)
+    # segment_ids=None: the plan of whole rows
+    plain = kda.kda_chunk_fwd_varlen(q, k, v, g, beta, None, B=B, T=T)
+    kda.kda_chunk_plan_varlen(None, B, T, H, D, D, dtype, ws)
+    o = kda.kda_chunk_fwd_varlen(q, k, v, g, beta, None, B=B, T=T, workspace=ws, planned=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, plain)
+
+
 def test_row_independence_and_determinism():
     B, T = 3, 300
     inp = _small_random(B, T, 2, 128, torch.bfloat16, seed=9, max_len=90)

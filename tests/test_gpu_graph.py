@@ -65,6 +65,68 @@ def test_step_captured_in_a_graph_matches_eager():
             assert torch.equal(a, b), f"trial {trial}: graph replay differs from eager: {name}"
 
 
+def test_two_stream_step_with_a_plan_matches_plain_calls():
+    """The bench's step shape: the scan and the chunk plan on a side stream of the graph,
+    beside the conv; the planned forward after the join. Replays on new inputs equal the
+    plain eager calls bit for bit."""
+    B, T, H, D, K = 2, 640, 4, 128, 4
+    F = H * D
+    dev = torch.device("cuda")
+    first = _small_random(B, T, H, D, torch.bfloat16, seed=41, max_len=200, pad_prob=0.05)
+    seg = first.segment_ids.to(dev).contiguous()
+    g, beta = first.g.to(dev).contiguous(), first.beta.to(dev).contiguous()
+    xs = [torch.randn(B, T, F, device=dev).bfloat16() for _ in range(3)]
+    w = (torch.randn(K, F, device=dev) * 0.5).bfloat16()
+    ys = [torch.empty_like(x) for x in xs]
+    cu = torch.empty(65, dtype=torch.int32, device=dev)
+    nseg = torch.empty(1, dtype=torch.int32, device=dev)
+    o = torch.empty(B * T, H, D, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(kda.chunk_fwd_workspace_bytes(B, T, H, D, D, torch.bfloat16), 256),
+                     dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream()
+
+    def step():
+        cur = torch.cuda.current_stream()
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            kda.kda_segids_to_cu_seqlens(seg, 64, out=cu, n_segs_out=nseg)
+            kda.kda_chunk_plan_varlen(seg, B, T, H, D, D, torch.bfloat16, ws)
+        for x, y in zip(xs, ys):
+            kda.kda_short_conv_varlen(x, w, seg, out=y)
+        cur.wait_stream(side)
+        qkv = [y.view(B * T, H, D) for y in ys]
+        kda.kda_chunk_fwd_varlen(qkv[0], qkv[1], qkv[2], g, beta, seg, B=B, T=T, out=o,
+                                 workspace=ws, planned=True)
+
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    for trial in range(3):
+        new = _small_random(B, T, H, D, torch.bfloat16, seed=50 + trial, max_len=120,
+                            pad_prob=0.05)
+        _fill(seg, new.segment_ids)
+        _fill(g, new.g)
+        _fill(beta, new.beta)
+        for x in xs:
+            x.copy_(torch.randn(B, T, F, device=dev).bfloat16())
+        graph.replay()
+        torch.cuda.synchronize()
+        cu_e, n_e = kda.kda_segids_to_cu_seqlens(seg, 64)
+        ys_e = [kda.kda_short_conv_varlen(x, w, seg) for x in xs]
+        o_e = kda.kda_chunk_fwd_varlen(*[y.view(B * T, H, D) for y in ys_e], g, beta, seg, B=B,
+                                       T=T)
+        torch.cuda.synchronize()
+        assert torch.equal(cu, cu_e) and torch.equal(nseg, n_e.reshape(nseg.shape))
+        for y, y_e in zip(ys, ys_e):
+            assert torch.equal(y, y_e)
+        assert torch.equal(o, o_e), f"trial {trial}: planned replay differs from the plain call"
+
+
 def test_backward_captured_in_a_graph_matches_eager():
     B, T, H, D = 2, 200, 2, 128
     dev = torch.device("cuda")

@@ -91,8 +91,8 @@ def chunk_flops_per_token_head(wl: synth.Workload) -> int:
 # `python bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline`. It holds only
 # for the kernel sources it was taken on (SHA-1 over the three files below);
 # after any change to them the bench reports null until a new capture.
-CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "bd37f7cc318680d5ce82a8c015bc545f2b04fe4f",
-                 "read": 558_399_232, "write": 116_986_624}
+CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "0b2b57ae2b539f995e531dde8036ec1134261fc6",
+                 "read": 557_805_056, "write": 116_805_632}
 CHUNK_SOURCES = ("kda_segids_cu_gb300/csrc/kda_chunk_tc.cu", "kda_segids_cu_gb300/csrc/kda_sm100.cuh",
                  "kda_segids_cu_gb300/csrc/kda_plan.cuh")
 

@@ -91,6 +91,7 @@ def chunk_flops_per_token_head(wl: synth.Workload) -> int:
 # `python bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline`. It holds only
 # for the kernel sources it was taken on (SHA-1 over the three files below);
 # after any change to them the bench reports null until a new capture.
+UNROLL = 8                         # steps per captured graph
 CHUNK_TRAFFIC = {"workload": "ling3", "sha1": "0b2b57ae2b539f995e531dde8036ec1134261fc6",
                  "read": 557_805_056, "write": 116_805_632}
 CHUNK_SOURCES = ("kda_segids_cu_gb300/csrc/kda_chunk_tc.cu", "kda_segids_cu_gb300/csrc/kda_sm100.cuh",
@@ -330,7 +331,7 @@ def run_gb300(args):
     # the convs; the forward joins it and takes the plan from the workspace.
     side = torch.cuda.Stream(device=dev)
 
-    def graph_step():
+    def graph_step(pair=None):
         cur = torch.cuda.current_stream()
         fork = torch.cuda.Event()
         fork.record(cur)
@@ -344,14 +345,53 @@ def run_gb300(args):
         for c, y in zip(convs, ys):
             kda.kda_short_conv_varlen(c.x, c.w, c.segment_ids, out=y)
         cur.wait_event(join)
+        if pair is not None:       # the forward may start: its inputs and plan are ready
+            ready = torch.cuda.Event()
+            ready.record(cur)
+            tstream.wait_event(ready)
+            pair[0].record(tstream)
         kda.kda_chunk_fwd_varlen(qkv[0], qkv[1], qkv[2], kin.g, kin.beta, seg, B=wl.B, T=wl.T,
                                  out=o, workspace=work, status=status, planned=True)
+        if pair is not None:       # the forward is done
+            done = torch.cuda.Event()
+            done.record(cur)
+            tstream.wait_event(done)
+            pair[1].record(tstream)
 
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        graph_step()
-    for _ in range(args.warmup):
-        graph.replay()
+    # The chunk kernel's duration inside the timed region: timing events recorded as nodes
+    # of the graph, on a stream of their own that waits for the point where the forward may
+    # start and for its end. No kernel depends on them (a record node in front of the
+    # forward would cut its programmatic launch after the last conv, about 6 us a step).
+    # One graph holds UNROLL steps (the same calls in sequence) and is replayed
+    # K // UNROLL times, then a one-step graph K % UNROLL times: after the timed loop the
+    # events hold the last timed launches. (Replaying one graph keeps the launch path warm;
+    # alternating between many graphs cost ~5 us per step.)
+    tstream = torch.cuda.Stream(device=dev)
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        timed_events = True
+    except TypeError:              # a torch without graph-node events: eager timing instead
+        timed_events = False
+
+    def capture(n_steps):
+        gr = torch.cuda.CUDAGraph()
+        prs = [tuple(torch.cuda.Event(enable_timing=True, external=True) for _ in range(2))
+               if timed_events else None for _ in range(n_steps)]
+        with torch.cuda.graph(gr):
+            tstream.wait_stream(torch.cuda.current_stream())
+            for pr in prs:
+                graph_step(pr)
+            torch.cuda.current_stream().wait_stream(tstream)
+        return gr, prs
+
+    unroll = min(UNROLL, args.steps)
+    g_many, pairs_many = capture(unroll)
+    rem = args.steps % unroll
+    g_one, pairs_one = capture(1) if rem else (None, [])
+    for _ in range(max(1, -(-args.warmup // unroll))):
+        g_many.replay()
+    if g_one is not None:
+        g_one.replay()
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
@@ -361,11 +401,15 @@ def run_gb300(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(args.steps):
-        graph.replay()
+    for _ in range(args.steps // unroll):
+        g_many.replay()
+    for _ in range(rem):
+        g_one.replay()
     t1.record(stream)
     torch.cuda.synchronize()
     clocks.mark_stop()
+    pairs = (pairs_many + pairs_one) if timed_events else []
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs) if pairs else None
     barrier(ws)
     clk = clocks.stop()
     ms_local = t0.elapsed_time(t1) / args.steps
@@ -508,7 +552,10 @@ def run_gb300(args):
     hbm, tf, tf_sus, peak_src = load_peaks()
     bytes_launch = chunk_bytes_per_token_head(wl) * N * H
     flops_launch = chunk_flops_per_token_head(wl) * N * H
-    achieved = bytes_launch / (chunk_ms / 1e3) / 1e9
+    # the dominant kernel's duration: timed in the graph when the events could be captured,
+    # else the eager call (planner + kernel)
+    dom_ms = kernel_ms if kernel_ms is not None else chunk_ms
+    achieved = bytes_launch / (dom_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
         "value": value,
@@ -527,10 +574,11 @@ def run_gb300(args):
                             "chunked KDA fwd" if seg is not None else
                             "3 causal short convs (producing q, k, v) + chunked KDA fwd "
                             "(segment_ids=None: no scan)"),
-                   "timing": ("the step's calls captured once in a CUDA graph, replayed K times "
-                              "between CUDA events (the scan and the chunk plan on a side stream "
-                              "of the graph, beside the convs); per-op times from an eager pass "
-                              "of the plain calls with events between them"),
+                   "timing": ("the step's calls captured in a CUDA graph (the scan and the chunk "
+                              "plan on a side stream of the graph, beside the convs; 8 steps per "
+                              "graph, each with timing events around the forward), K steps "
+                              "replayed between CUDA events; per-op times from an eager pass of "
+                              "the plain calls with events between them"),
                    "l2": (f"inputs larger than L2 (conv inputs "
                           f"{sum(c.x.numel() * c.x.element_size() for c in convs) / 1e6:.0f} MB, "
                           f"g and beta "
@@ -539,10 +587,13 @@ def run_gb300(args):
                    "parallelism": f"replicas x{ws} (rows independent)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": chunk_traffic(wl),
-                     "kernel": "kda_chunk_fwd_varlen (planner + chunk kernel)",
-                     "chunk_ms": chunk_ms, "bytes_per_launch": bytes_launch,
-                     "flops_per_launch": flops_launch,
-                     "tensor_frac": flops_launch / (chunk_ms / 1e3) / (tf * 1e12),
+                     "kernel": ("tc::chunk_kernel (kda_chunk_fwd_varlen_planned), timed by "
+                                f"events in the graph, mean of the last {len(pairs)} timed "
+                                "steps" if kernel_ms is not None else
+                                "kda_chunk_fwd_varlen (planner + chunk kernel), eager pass"),
+                     "kernel_ms": dom_ms, "chunk_ms": chunk_ms,
+                     "bytes_per_launch": bytes_launch, "flops_per_launch": flops_launch,
+                     "tensor_frac": flops_launch / (dom_ms / 1e3) / (tf * 1e12),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
         "ops": {
             name: {"us_per_call": ms_ * 1e3, "algorithmic_bytes": nbytes,

@@ -587,9 +587,11 @@ def run_gb300(args):
                    "parallelism": f"replicas x{ws} (rows independent)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": chunk_traffic(wl),
-                     "kernel": ("tc::chunk_kernel (kda_chunk_fwd_varlen_planned), timed by "
-                                f"events in the graph, mean of the last {len(pairs)} timed "
-                                "steps" if kernel_ms is not None else
+                     "kernel": (("tc::chunk_kernel" if wl.dtype == torch.bfloat16 and
+                                 wl.d_qk == 128 else "the token-recurrence kernels") +
+                                " (kda_chunk_fwd_varlen_planned), timed by events in the graph, "
+                                f"mean of the last {len(pairs)} timed steps"
+                                if kernel_ms is not None else
                                 "kda_chunk_fwd_varlen (planner + chunk kernel), eager pass"),
                      "kernel_ms": dom_ms, "chunk_ms": chunk_ms,
                      "bytes_per_launch": bytes_launch, "flops_per_launch": flops_launch,

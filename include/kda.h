@@ -298,17 +298,21 @@ kda_status_t kda_chunk_bwd_varlen(const void *q, const void *k, const void *v, c
  * exits. It allocates nothing and calls no allocating routine.
  *
  * Arguments, layouts and results are those of kda_chunk_fwd_varlen without the
- * workspace pair. Problems whose kda_chunk_fwd_varlen_workspace_size exceeds
+ * workspace pair, and the arguments are checked in the same order, so a null
+ * or misaligned tensor returns KDA_ERR_INVALID_ARG whatever the size. Then
+ * problems whose kda_chunk_fwd_varlen_workspace_size exceeds
  * KDA_NOALLOC_SCRATCH_BYTES are refused with KDA_ERR_WORKSPACE before anything
  * is launched (the 4 MiB array covers up to 524,256 tokens, B*T, for either
  * dtype).
  *
  * The first call on a device looks up the array's device address on that
  * device (with it current) and caches it; make that first call before any
- * stream capture. Every call shares the one array and leaves its contents
- * behind; the kernels rewrite all scratch they read, so stale contents do not
- * matter, but calls whose kernels overlap on the GPU race on the array: issue
- * them on one stream, or order them.
+ * stream capture. A lookup that fails returns KDA_ERR_CUDA and is not cached:
+ * the next call on that device tries again. Every call shares the one array
+ * and leaves its contents behind; the kernels write every scratch word before
+ * they read it, so stale contents do not matter, but calls whose kernels
+ * overlap on the GPU race on the array: issue them on one stream, or order
+ * them.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES (4u << 20)
 

@@ -27,6 +27,7 @@ KDA_OK = 0
 KDA_F32 = 0
 KDA_BF16 = 1
 KDA_DEV_DECAY_RANGE = 0x1
+KDA_DEV_TIMEOUT = 0x2
 
 _lib = None
 
@@ -36,6 +37,17 @@ class KdaError(RuntimeError):
         self.status = status
         name = load_library().kda_status_string(status).decode()
         super().__init__(f"{fn} failed: {name} ({status})")
+
+
+class KdaDeviceError(RuntimeError):
+    """A condition the kernels reported through the device status word (KDA_DEV_* bits)."""
+
+    def __init__(self, fn: str, bits: int):
+        self.bits = bits
+        names = [n for b, n in ((KDA_DEV_DECAY_RANGE, "KDA_DEV_DECAY_RANGE"),
+                                (KDA_DEV_TIMEOUT, "KDA_DEV_TIMEOUT")) if bits & b]
+        super().__init__(f"{fn}: device status {bits:#x} ({', '.join(names) or 'unknown'}); "
+                         "the outputs of this call are unreliable")
 
 
 def load_library(path: str | None = None) -> ctypes.CDLL:
@@ -116,6 +128,33 @@ def _ptr(t: torch.Tensor | None):
 def _check(fn: str, status: int) -> None:
     if status != KDA_OK:
         raise KdaError(fn, status)
+
+
+def _status_word(status: torch.Tensor | None, check: bool | None, device, stream):
+    """The device status word of a forward call and whether the wrapper reads it.
+
+    check=None (the default) reads it when the wrapper owns the word (status is None) and
+    the stream is not being captured; check=True always reads it (not under capture);
+    check=False never does. Reading means waiting for the stream."""
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    capturing = torch.cuda.is_current_stream_capturing()
+    if check is None:
+        check = status is None and not capturing
+    elif check and capturing:
+        raise ValueError("check=True cannot wait under stream capture: pass a status tensor "
+                         "and read it after the graph runs")
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+    elif check:
+        status.zero_()
+    return status, check, s
+
+
+def _raise_on_status(fn: str, status: torch.Tensor, stream) -> None:
+    stream.synchronize()
+    bits = int(status.item()) & 0xffffffff
+    if bits:
+        raise KdaDeviceError(fn, bits)
 
 
 def kda_segids_to_cu_seqlens(segment_ids: torch.Tensor, max_segs: int, stream=None,
@@ -218,22 +257,32 @@ def kda_chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: t
                          workspace: torch.Tensor | None = None,
                          status: torch.Tensor | None = None,
                          out_dtype: torch.dtype | None = None,
-                         planned: bool = False) -> torch.Tensor:
+                         planned: bool = False, check: bool | None = None) -> torch.Tensor:
     """Packed KDA forward. q, k, g: [B, T, H, Dk], [1, B*T, H, Dk] or [B*T, H, Dk];
     v like q with Dv; beta [..., H]; segment_ids int32 [B, T] or None.
     Returns o shaped like v, of `out_dtype` (default: the input dtype; float32
     is also accepted). planned=True skips the planning: `workspace` must hold the
-    plan of these segment ids and sizes from kda_chunk_plan_varlen."""
+    plan of these segment ids and sizes from kda_chunk_plan_varlen.
+
+    Device-side conditions (KDA_DEV_* bits) go to `status`, an int32 device tensor
+    ORed into and never cleared by the kernels. By default (status None, check None)
+    the wrapper allocates the word, waits for the stream after the launch and raises
+    KdaDeviceError if a bit is set. Pass check=False to skip that wait (the word is
+    then the caller's to read), or pass your own `status` to read it yourself; under
+    stream capture the wrapper never waits."""
     if planned and workspace is None:
         raise ValueError("planned=True needs the workspace that holds the plan")
     q, k, v, g, beta, seg, B, T, H, Dk, Dv, dt, odt, o, workspace = _chunk_args(
         q, k, v, g, beta, segment_ids, B, T, out, workspace, out_dtype)
+    status, check, st = _status_word(status, check, q.device, stream)
     lib = load_library()
     fn, name = ((lib.kda_chunk_fwd_varlen_planned, "kda_chunk_fwd_varlen_planned") if planned
                 else (lib.kda_chunk_fwd_varlen, "kda_chunk_fwd_varlen"))
     _check(name, fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(seg), B, T, H, Dk, Dv,
                     float(scale), dt, odt, _ptr(o), _ptr(workspace), workspace.numel(),
-                    _ptr(status), _stream_ptr(stream)))
+                    _ptr(status), _stream_ptr(st)))
+    if check:
+        _raise_on_status(name, status, st)
     return o
 
 
@@ -265,14 +314,16 @@ def kda_chunk_fwd_varlen_state(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
                                stream=None, out: torch.Tensor | None = None,
                                workspace: torch.Tensor | None = None,
                                status: torch.Tensor | None = None,
-                               out_dtype: torch.dtype | None = None):
+                               out_dtype: torch.dtype | None = None,
+                               check: bool | None = None):
     """kda_chunk_fwd_varlen with per-segment state: segment r (flattened token order,
     as in cu_seqlens) starts from initial_state[r] ([n_state, H, Dk, Dv] float32) and,
     with output_final_state, its state after its last token is returned in
     final[r]. n_state defaults to initial_state's first dimension (else 0).
-    Returns (o, final or None)."""
+    Returns (o, final or None). `status` and `check` as in kda_chunk_fwd_varlen."""
     q, k, v, g, beta, seg, B, T, H, Dk, Dv, dt, odt, o, workspace = _chunk_args(
         q, k, v, g, beta, segment_ids, B, T, out, workspace, out_dtype)
+    status, check, st = _status_word(status, check, q.device, stream)
     if n_state is None:
         n_state = initial_state.shape[0] if initial_state is not None else 0
     init = None
@@ -287,7 +338,9 @@ def kda_chunk_fwd_varlen_state(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
            load_library().kda_chunk_fwd_varlen_state(
                _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(seg), B, T, H, Dk, Dv,
                float(scale), dt, odt, _ptr(o), _ptr(init), _ptr(fin), int(n_state),
-               _ptr(workspace), workspace.numel(), _ptr(status), _stream_ptr(stream)))
+               _ptr(workspace), workspace.numel(), _ptr(status), _stream_ptr(st)))
+    if check:
+        _raise_on_status("kda_chunk_fwd_varlen_state", status, st)
     return o, fin
 
 
@@ -344,4 +397,4 @@ def kda_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tenso
 __all__ = ["kda_segids_to_cu_seqlens", "kda_short_conv_varlen", "kda_chunk_fwd_varlen",
            "kda_chunk_plan_varlen", "kda_chunk_fwd_varlen_state", "kda_chunk_bwd_varlen", "kda_varlen",
            "chunk_fwd_workspace_bytes", "load_library", "header_functions", "KdaError",
-           "KDA_DEV_DECAY_RANGE"]
+           "KdaDeviceError", "KDA_DEV_DECAY_RANGE", "KDA_DEV_TIMEOUT"]

@@ -42,6 +42,31 @@ bool token_count_ok(int64_t B, int64_t T) {
 
 }  // namespace
 
+namespace kda {
+
+// The checks of the inputs and outputs that every forward entry point shares (all of
+// kda_chunk_fwd_varlen's checks but the workspace's), in the order kda.h documents.
+kda_status_t check_fwd_inputs(const void* q, const void* k, const void* v, const void* g,
+                              const void* beta, const int32_t* segment_ids, int64_t B, int64_t T,
+                              int32_t H, int32_t d_qk, int32_t d_v, kda_dtype_t dtype,
+                              kda_dtype_t out_dtype, const void* o, const uint32_t* status_dev) {
+    if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !valid_dtype(out_dtype) || !token_count_ok(B, T) || H < 1 ||
+        d_qk < 1 || d_v < 1)
+        return KDA_ERR_INVALID_ARG;
+    if (out_dtype != dtype && out_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return KDA_ERR_UNSUPPORTED;
+    if (int64_t(H) * d_qk > 65536) return KDA_ERR_UNSUPPORTED;
+    const void* ptrs[] = {q, k, v, g, beta, o};
+    for (const void* p : ptrs)
+        if (!kda::aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (segment_ids && !kda::aligned(segment_ids, 4)) return KDA_ERR_INVALID_ARG;
+    if (status_dev && !kda::aligned(status_dev, 4)) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+}  // namespace kda
+
 extern "C" {
 
 const char* kda_status_string(kda_status_t s) {
@@ -92,6 +117,7 @@ size_t kda_chunk_fwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int3
     return tc > rec ? tc : rec;
 }
 
+
 namespace {
 
 // The checks kda_chunk_fwd_varlen and kda_chunk_fwd_varlen_planned share.
@@ -100,18 +126,9 @@ kda_status_t check_fwd_args(const void* q, const void* k, const void* v, const v
                             int32_t H, int32_t d_qk, int32_t d_v, kda_dtype_t dtype,
                             kda_dtype_t out_dtype, const void* o, const void* workspace,
                             size_t workspace_bytes, const uint32_t* status_dev) {
-    if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
-    if (!valid_dtype(dtype) || !valid_dtype(out_dtype) || !token_count_ok(B, T) || H < 1 ||
-        d_qk < 1 || d_v < 1)
-        return KDA_ERR_INVALID_ARG;
-    if (out_dtype != dtype && out_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
-    if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return KDA_ERR_UNSUPPORTED;
-    if (int64_t(H) * d_qk > 65536) return KDA_ERR_UNSUPPORTED;
-    const void* ptrs[] = {q, k, v, g, beta, o};
-    for (const void* p : ptrs)
-        if (!kda::aligned(p, 16)) return KDA_ERR_INVALID_ARG;
-    if (segment_ids && !kda::aligned(segment_ids, 4)) return KDA_ERR_INVALID_ARG;
-    if (status_dev && !kda::aligned(status_dev, 4)) return KDA_ERR_INVALID_ARG;
+    const kda_status_t s = kda::check_fwd_inputs(q, k, v, g, beta, segment_ids, B, T, H, d_qk,
+                                                 d_v, dtype, out_dtype, o, status_dev);
+    if (s != KDA_OK) return s;
     const size_t need = kda_chunk_fwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
     if (!workspace || workspace_bytes < need || !kda::aligned(workspace, 256))
         return KDA_ERR_WORKSPACE;

@@ -3,8 +3,8 @@
 Bar (per head, over real tokens): max|o - o_ref| <= 2e-2 RMS(o_ref) for bf16
 inputs, <= 1e-4 RMS(o_ref) for fp32 inputs; padding outputs exactly 0.
 Small workloads are compared in full; the large ones at their full size, in
-the launch configuration the bench times, on sampled heads that the oracle
-computes in seconds. Bit-exact invariants: documents do not leak into each
+the launch configuration the bench times: ling3 and short on every head, the
+long workloads on sampled heads that the oracle computes in seconds. Bit-exact invariants: documents do not leak into each
 other, rows are independent, segment_ids=None equals all-ones ids, reruns are
 deterministic. Within the bound: a packed call equals its documents run alone.
 """
@@ -52,9 +52,10 @@ def test_small_workloads_full(name):
     check_kda_output(o, ref, inp.segment_ids, wl.dtype, label=name)
 
 
-@pytest.mark.parametrize("name,heads", [("ling3", [0, 7, 15]), ("short", [0, 15]),
+@pytest.mark.parametrize("name,heads", [("ling3", None), ("short", None),
                                         ("long", [0, 31]), ("long_none", [5])])
-def test_large_workloads_sampled_heads(name, heads):
+def test_large_workloads(name, heads):
+    """ling3 and short on every head; long and long_none on sampled heads."""
     wl = synth.WORKLOADS[name]
     inp = synth.make_kda_inputs(wl, device="cuda")
     ref = _oracle(inp, wl.B, wl.T, heads=heads)
@@ -111,7 +112,8 @@ def test_boundary_sweep(dtype, D):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_every_boundary_offset(dtype):
-    # one document boundary at each offset 1..64 of the second chunk
+    # one document boundary at each offset 1..64 of the second chunk (64-wide heads: the
+    # token recurrence)
     for off in range(1, 65):
         T = 192
         seg = torch.ones(1, T, dtype=torch.int32)
@@ -119,6 +121,28 @@ def test_every_boundary_offset(dtype):
         inp = _small_random(1, T, 1, 64, dtype, seed=off)
         inp.segment_ids = seg
         check_kda_output(_gpu_fwd(inp, 1, T), _oracle(inp, 1, T), seg, dtype, label=f"off{off}")
+
+
+@pytest.mark.parametrize("out_dtype", [None, torch.float32])
+def test_every_boundary_offset_tensor_core(out_dtype):
+    """bf16 with 128-wide heads (the tcgen05 kernel): a boundary at each offset 0..63 of a
+    chunk in two rows whose second row starts inside a chunk (T = 200: flat 200 is offset 8
+    of chunk 3), plus a boundary on the first and on the last row of another chunk and a
+    padding run, so that row masks, the A' mask, first cuts and carried states all see
+    every in-chunk position."""
+    B, T, H = 2, 200, 2
+    for off in range(64):
+        seg = torch.ones(B, T, dtype=torch.int32)
+        seg[0, 64 + off:] = 2                  # row 0: chunk 1, offset off
+        seg[0, 128:] = 3                       # row 0: first row of chunk 2
+        seg[0, 191:] = 4                       # row 0: last row of chunk 2
+        seg[1, 56 + off:] = 5                  # row 1 (flat 200..399): chunk 4, offset off
+        seg[1, 120 + (off % 7):126 + (off % 7)] = 0     # padding inside chunk 5
+        inp = _small_random(B, T, H, 128, torch.bfloat16, seed=500 + off)
+        inp.segment_ids = seg
+        o = _gpu_fwd(inp, B, T, scale=0.75, out_dtype=out_dtype)
+        check_kda_output(o, _oracle(inp, B, T, scale=0.75), seg, torch.bfloat16,
+                         label=f"tc off{off}")
 
 
 def test_isolation_bitwise():

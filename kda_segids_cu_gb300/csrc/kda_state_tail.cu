@@ -174,20 +174,52 @@ __device__ void head_output(const Tile& t, int r, int end, const float* __restri
             }
         }
     }
-    __syncthreads();
+    // Kd's factor exp(G_{r-1} - G_j) leaves fp32's range once a key channel decays by more
+    // than e^-80 over the segment's rows here; the scores are then formed from one
+    // exponential per (t, j, channel) instead, which has no range limit.
+    bool big = false;
+    if (tid < kTD) {
+        const float gr = r > 0 ? t.G[(r - 1) * kTD + tid] : 0.f;
+        big = !(t.G[(end - 1) * kTD + tid] - gr >= -80.f);
+    }
+    const bool strong = __syncthreads_or(big) != 0;   // also orders W and X before their reads
     {                                             // A[j][t] = Qd_t . Kd_j for r <= j <= t < end
         const int ta = tid >> 4, jb = tid & 15;   // rows t 2 ta, 2 ta + 1; columns j 4 jb .. +3
         float acc[2][4] = {};
         if (2 * ta + 1 >= r && 2 * ta < end && 4 * jb < end && 4 * jb <= 2 * ta + 1) {
+            if (!strong) {
 #pragma unroll 4
-            for (int c = 0; c < kTD; ++c) {
-                const float2 w = *reinterpret_cast<const float2*>(t.W + c * kTR + 2 * ta);
-                const float4 x = *reinterpret_cast<const float4*>(t.X + c * kTR + 4 * jb);
-                const float wv[2] = {w.x, w.y}, xv[4] = {x.x, x.y, x.z, x.w};
+                for (int c = 0; c < kTD; ++c) {
+                    const float2 w = *reinterpret_cast<const float2*>(t.W + c * kTR + 2 * ta);
+                    const float4 x = *reinterpret_cast<const float4*>(t.X + c * kTR + 4 * jb);
+                    const float wv[2] = {w.x, w.y}, xv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
+                    for (int i = 0; i < 2; ++i)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(wv[i], xv[j], acc[i][j]);
+                        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(wv[i], xv[j], acc[i][j]);
+                }
+            } else {
+                // q_tc k_jc exp(G_tc - G_jc), channels taken from a per-thread offset so that
+                // the threads of a warp read different banks; the exponent is capped at 0
+                // (pairs j > t are discarded below)
+                for (int c0 = 0; c0 < kTD; ++c0) {
+                    const int c = (c0 + jb) & (kTD - 1);
+                    float gt[2], qt[2];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        gt[i] = t.G[(2 * ta + i) * kTD + c];
+                        qt[i] = __bfloat162float(t.q[(2 * ta + i) * kTD + c]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int jj = 4 * jb + j;
+                        const float gj = t.G[jj * kTD + c];
+                        const float kj = t.beta[jj] * __bfloat162float(t.k[jj * kTD + c]);
+#pragma unroll
+                        for (int i = 0; i < 2; ++i)
+                            acc[i][j] = fmaf(qt[i] * kj, expf(fminf(gt[i] - gj, 0.f)), acc[i][j]);
+                    }
+                }
             }
         }
 #pragma unroll

@@ -218,3 +218,132 @@ def chunked_forward_state(q, k, v, g, beta, seg, B, T, init=None, n_state=0, wan
                 if want_final and ends_here:
                     fin[rank, h] = final(r, end - 1, None if S0 is None else S0[rank, h])
     return torch.from_numpy(o), (None if fin is None else torch.from_numpy(fin))
+
+
+def chunk_units(first_cut, cuts=None):
+    """Units of the tensor-core kernel's plan: a unit runs from a cut chunk (from its first
+    start-or-padding row) to the next cut chunk (up to that chunk's first cut row).
+    `cuts` (chunk indices, sorted) defaults to every chunk holding a start or padding; the
+    first of those is always included. Returns [(c0, c1, row_lo, row_hi)]."""
+    n_chunks = len(first_cut)
+    cand = [c for c in range(n_chunks) if first_cut[c] < C]
+    cuts = cand if cuts is None else sorted(set(cuts) | {cand[0]})
+    units = []
+    for i, c0 in enumerate(cuts):
+        if i + 1 < len(cuts):
+            cn = cuts[i + 1]
+            sn = first_cut[cn]
+            c1, row_hi = (cn, sn) if sn > 0 else (cn - 1, C)
+        else:
+            c1, row_hi = n_chunks - 1, C
+        units.append((c0, c1, int(first_cut[c0]), row_hi))
+    return units
+
+
+def chunked_forward_units(q, k, v, g, beta, seg, B, T, scale=1.0, cuts=None, mode="auto",
+                          group_floor=-10.0):
+    """The tensor-core kernel's algebra in float64, unit by unit, with its masks and its two
+    forms. Per chunk: Suf_i sums g over the real rows after i up to the chunk's end (the
+    whole-chunk form) or up to the end of row i's 16-row sub-block (the sub-block form,
+    taken when `mode` is "always", or for "auto" when some channel's sum over an 8-row group
+    falls below `group_floor`); Qt = q exp(-Suf), Ktb = beta k exp(Suf); A' = the masked
+    Qt Ktb^T (only the diagonal 16x16 blocks in the sub-block form); O = A' V plus the
+    read-out of the incoming state, and the state update, once per chunk or once per
+    sub-block with the sub-block's masks (in_b, Kh' rows from the last start, Qt rows before
+    the first cut). Each unit starts from a zero state; rows outside [row_lo, row_hi) of its
+    first and last chunks belong to the neighbouring units. Returns (o [N, H, Dv] float64,
+    the number of chunk-heads that took the sub-block form)."""
+    f = (lambda t: t.detach().to(torch.float64).numpy()) if isinstance(q, torch.Tensor) else np.asarray
+    q, k, v, g, beta = (f(t) for t in (q, k, v, g, beta))
+    N, H, Dk = q.shape
+    Dv = v.shape[-1]
+    ids = np.ones(N, dtype=np.int64) if seg is None else \
+        (seg.numpy() if isinstance(seg, torch.Tensor) else np.asarray(seg)).reshape(-1)
+    p = np.arange(N)
+    valid_all = ids != 0
+    prev = np.concatenate([[0], ids[:-1]])
+    start_all = valid_all & ((p % T == 0) | (ids != prev))
+    n_chunks = (N + C - 1) // C
+    masks = []
+    first_cut = np.zeros(n_chunks, int)
+    for c in range(n_chunks):
+        lo_p, hi_p = c * C, min((c + 1) * C, N)
+        valid = np.zeros(C, bool)
+        start = np.zeros(C, bool)
+        valid[: hi_p - lo_p] = valid_all[lo_p:hi_p]
+        start[: hi_p - lo_p] = start_all[lo_p:hi_p]
+        masks.append((valid, start))
+        cut = np.nonzero(start | ~valid)[0]
+        first_cut[c] = cut[0] if len(cut) else C
+    rows = np.arange(C)
+    o = np.zeros((N, H, Dv))
+    n_sub = 0
+
+    def rows_of(c, h, arr):
+        lo_p, hi_p = c * C, min((c + 1) * C, N)
+        out = np.zeros((C,) + arr.shape[2:])
+        out[: hi_p - lo_p] = arr[lo_p:hi_p, h]
+        return out
+
+    for (c0, c1, row_lo, row_hi) in chunk_units(first_cut, cuts):
+        for h in range(H):
+            S = np.zeros((Dk, Dv))
+            for c in range(c0, c1 + 1):
+                valid, start = masks[c]
+                unit_first = c == c0
+                lo_row = row_lo if unit_first else 0
+                hi_row = row_hi if c == c1 else C
+                fc = first_cut[c]
+                starts = np.nonzero(start)[0]
+                last_start = starts[-1] if len(starts) else 0
+                tail_live = valid[C - 1]
+                read_state = (not unit_first) and fc > 0
+                carry = (not unit_first) and fc == C
+                gg = np.where(valid[:, None], rows_of(c, h, g), 0.0)
+                groups = gg.reshape(8, 8, Dk).sum(axis=1)
+                sub = mode == "always" or (mode == "auto" and bool((groups < group_floor).any()))
+                n_sub += int(sub)
+                span = 16 if sub else C
+                Suf = np.zeros((C, Dk))
+                for i in range(C):
+                    end = (i // span + 1) * span
+                    Suf[i] = gg[i + 1:end].sum(axis=0)
+                qq, kk, vv, bb = rows_of(c, h, q), rows_of(c, h, k), rows_of(c, h, v), rows_of(c, h, beta)
+                Qt = np.where(valid[:, None], qq * np.exp(-Suf), 0.0)
+                Ktb = np.where(valid[:, None], kk * bb[:, None] * np.exp(Suf), 0.0)
+                lo = np.array([(np.nonzero(start[: i + 1])[0][-1] if start[: i + 1].any() else 0)
+                               for i in range(C)])
+                if sub:
+                    lo = np.maximum(lo, rows // 16 * 16)
+                jj = rows[None, :]
+                keep = valid[:, None] & (jj >= lo[:, None]) & (jj <= rows[:, None])
+                O = np.where(keep, Qt @ Ktb.T, 0.0) @ vv
+                if not sub:
+                    kh_lo = last_start if tail_live else C
+                    q_hi = fc if (read_state and fc < C) else C
+                    P = np.exp(gg.sum(axis=0))
+                    if read_state:
+                        O += np.where((rows < q_hi)[:, None], Qt, 0.0) @ (P[:, None] * S)
+                    Snew = np.where((rows >= kh_lo)[:, None], Ktb, 0.0).T @ vv
+                    if carry:
+                        Snew += P[:, None] * S
+                    S = Snew
+                else:
+                    for b in range(4):
+                        rb = slice(16 * b, 16 * b + 16)
+                        stb, vab = start[rb], valid[rb]
+                        cutb = stb | ~vab
+                        in_b = (not unit_first) or 16 * b > lo_row
+                        kh_lo = (16 * b + (np.nonzero(stb)[0][-1] if stb.any() else 0)) if vab[-1] else C
+                        q_hi = 16 * b + np.nonzero(cutb)[0][0] if (in_b and cutb.any()) else C
+                        P = np.exp(gg[rb].sum(axis=0))
+                        Sdec = P[:, None] * S if in_b else np.zeros((Dk, Dv))
+                        O[rb] += np.where((rows[rb] < q_hi)[:, None], Qt[rb], 0.0) @ Sdec
+                        Snew = np.where((rows[rb] >= kh_lo)[:, None], Ktb[rb], 0.0).T @ vv[rb]
+                        if in_b and not cutb.any():
+                            Snew += P[:, None] * S
+                        S = Snew
+                lo_p = c * C
+                for i in range(lo_row, min(hi_row, N - lo_p)):
+                    o[lo_p + i, h] = scale * O[i]
+    return torch.from_numpy(o), n_sub

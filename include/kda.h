@@ -56,8 +56,8 @@ typedef enum {
 } kda_dtype_t;
 
 /* Bits that kda_chunk_fwd_varlen ORs into *status_dev. */
-#define KDA_DEV_DECAY_RANGE 0x1u /* a chunk's cumulative log-decay left the range
-                                    the chunked factorisation handles (see below) */
+#define KDA_DEV_DECAY_RANGE 0x1u /* a 16-token block's cumulative log-decay left the
+                                    range the chunked factorisation handles (see below) */
 #define KDA_DEV_TIMEOUT 0x2u     /* a bounded in-kernel wait (TMA or tensor-core
                                     completion) gave up; outputs are incomplete */
 
@@ -138,11 +138,16 @@ size_t kda_chunk_fwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int3
  * fp32 arithmetic. Supported: d_qk == d_v in {64, 128}; H >= 1.
  *
  * The chunked form factors the in-chunk decay into per-token scalings
- * exp(G_i - G_last) and exp(G_last - G_j), G the cumulative log-decay in
- * the chunk. If some channel's cumulative log-decay over one chunk falls
- * below -80 (for instance g < -1.25 on every token of a chunk) those factors
- * leave fp32's range; the kernel then sets KDA_DEV_DECAY_RANGE in
- * *status_dev and the affected outputs are unreliable.
+ * exp(G_i - G_ref) and exp(G_ref - G_j), G the cumulative log-decay in the
+ * chunk and G_ref its value at the chunk's end. Where some channel's log-decay
+ * over a chunk falls below -80 (for instance g < -1.25 on every token) those
+ * factors would leave fp32's range; such chunks are computed again with a
+ * reference point at the end of each 16-token block instead, which holds
+ * while every channel's log-decay over each 16-token block stays above -80
+ * (a per-token average above -5). Past that the kernel sets
+ * KDA_DEV_DECAY_RANGE in *status_dev and the affected outputs are
+ * unreliable. (fp32 inputs and 64-wide heads run the token recurrence, which
+ * has no such limit.)
  *
  *   workspace        device scratch of at least
  *                    kda_chunk_fwd_varlen_workspace_size(...) bytes, 256-byte

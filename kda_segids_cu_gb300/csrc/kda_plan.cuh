@@ -15,7 +15,8 @@ struct ChunkMeta {
 struct Plan {                      // device view of the workspace
     int32_t* counters;             // [0] n_units, [1] next item, [2] n_chunks, [3] n_active,
                                    // [4] next unit of the state pass, [5] chunk-kernel CTAs
-                                   // finished (the last one rewinds [1] and [5])
+                                   // finished (the last one rewinds [1] and [5]), [6] units
+                                   // the fast chunk kernel left to the safe one
     ChunkMeta* meta;               // [n_chunks]
     int32_t* first_cut;            // [n_chunks] first start-or-padding row, 64 if none
     int32_t* block_cut;            // [n_blocks]
@@ -25,6 +26,9 @@ struct Plan {                      // device view of the workspace
     int32_t* rank_base;            // [n_chunks] segment starts before the chunk (state calls only)
     int32_t* active;               // [n_chunks] chunks holding a start or a carried segment's end
                                    // (state calls only), in order
+    int32_t* redo;                 // [n_chunks] positions (in order) of the units left to the
+                                   // safe chunk kernel, counters[6] of them
+    int32_t* redo_flag;            // [n_chunks] per position: 1 once listed in redo
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -32,8 +36,8 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 __host__ __device__ inline size_t plan_bytes(int64_t n_chunks) {
     size_t b = align256(64 * sizeof(int32_t));
     b += align256(n_chunks * sizeof(ChunkMeta));
-    b += align256(n_chunks * sizeof(int32_t)) * 6;   // first_cut, block_cut, cut_list, order,
-                                                     // rank_base, active
+    b += align256(n_chunks * sizeof(int32_t)) * 8;   // first_cut, block_cut, cut_list, order,
+                                                     // rank_base, active, redo, redo_flag
     b += align256(n_chunks * sizeof(int4));
     return b;
 }
@@ -49,6 +53,8 @@ __host__ __device__ inline Plan plan_view(void* ws, int64_t n_chunks) {
     pl.order = reinterpret_cast<int32_t*>(p);         p += align256(n_chunks * sizeof(int32_t));
     pl.rank_base = reinterpret_cast<int32_t*>(p);     p += align256(n_chunks * sizeof(int32_t));
     pl.active = reinterpret_cast<int32_t*>(p);        p += align256(n_chunks * sizeof(int32_t));
+    pl.redo = reinterpret_cast<int32_t*>(p);          p += align256(n_chunks * sizeof(int32_t));
+    pl.redo_flag = reinterpret_cast<int32_t*>(p);     p += align256(n_chunks * sizeof(int32_t));
     pl.units = reinterpret_cast<int4*>(p);
     return pl;
 }

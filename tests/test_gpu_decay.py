@@ -3,10 +3,12 @@
 The tensor-core kernel factorises exp(G_i - G_j) as exp(-Suf_i) exp(Suf_j). With a
 reference point at the chunk's end, that leaves fp32's range once a key channel
 decays by more than about e^-80 over a chunk (a per-token average below -1.25).
-Such chunks take the sub-block form, with the reference at the end of each 16-row
-sub-block; that holds while every 16-row sub-block stays above e^-80 (an average
-above -5 per token). RFC-0026 §3.3's gate kwargs (lower_bound, safe_gate) are there
-for gates this strong.
+The fast chunk kernel has only that form; it lists the units holding such a chunk,
+and the safe chunk kernel, launched after it, reruns those units with the choice of
+the sub-block form per chunk: the reference at the end of each 16-row sub-block,
+which holds while every 16-row sub-block stays above e^-80 (an average above -5 per
+token). RFC-0026 §3.3's gate kwargs (lower_bound, safe_gate) are there for gates
+this strong.
 
 - Decay of about -3 per token (range -1.5 .. -4.5) on some channels, mixed with the
   usual decay on the others, on layouts with boundaries at every sub-block position,
@@ -157,4 +159,46 @@ def test_decay_beyond_the_range_is_reported():
     status.zero_()
     kda.kda_chunk_fwd_varlen(*(t.cuda() for t in (q, k, v, g, beta)), seg.cuda(), status=status)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+
+def test_strong_decay_planned_calls_and_graph_replay():
+    """The fast chunk kernel leaves units with a chunk out of its range to the safe kernel,
+    through a list in the workspace that the safe kernel empties again. Planned calls that
+    reuse one plan, alternating strong and usual decay, and replays of a captured forward
+    each equal the plain call bit for bit."""
+    B, T, H, D = 2, 640, 3, 128
+    rng = np.random.default_rng(9)
+    seg = torch.from_numpy(synth.random_segment_ids(rng, B, T, max_len=400, pad_prob=0.05))
+    strong = [t.cuda() for t in _strong_inputs(seg, H, D, torch.bfloat16, seed=5)]
+    usual = [t.cuda() for t in _strong_inputs(seg, H, D, torch.bfloat16, seed=6, n_strong=0)]
+    segd = seg.cuda()
+    ws = torch.empty(max(kda.chunk_fwd_workspace_bytes(B, T, H, D, D, torch.bfloat16), 256),
+                     dtype=torch.uint8, device="cuda")
+    kda.kda_chunk_plan_varlen(segd, B, T, H, D, D, torch.bfloat16, ws)
+    for inp in (strong, usual, strong, strong, usual):
+        plain = kda.kda_chunk_fwd_varlen(*inp, segd)
+        o = kda.kda_chunk_fwd_varlen(*inp, segd, workspace=ws, planned=True)
+        torch.cuda.synchronize()
+        assert torch.equal(o, plain)
+    ref = oracle.kda_fwd(*(t.cpu() for t in strong), seg, B, T)
+    check_kda_output(kda.kda_chunk_fwd_varlen(*strong, segd), ref, seg, torch.bfloat16,
+                     label="planned strong")
+    # a captured planned forward, replayed on strong then usual inputs
+    bufs = [t.clone() for t in strong]
+    out = torch.empty_like(bufs[2])
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        kda.kda_chunk_fwd_varlen(*bufs, segd, workspace=ws, planned=True, out=out, status=status)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        kda.kda_chunk_fwd_varlen(*bufs, segd, workspace=ws, planned=True, out=out, status=status)
+    for inp in (strong, usual, strong):
+        for dst, src in zip(bufs, inp):
+            dst.copy_(src)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, kda.kda_chunk_fwd_varlen(*inp, segd))
     assert int(status.item()) == 0

@@ -6,10 +6,17 @@ properties, allocates outputs and workspace with torch, and passes device
 pointers plus the current CUDA stream. There is no CPU fallback: if
 libkda.so is missing or a call fails, an exception is raised.
 
-Calls (same names as the C ABI):
+Calls (same names as the C ABI; segids_to_cu_seqlens, short_conv_varlen and
+chunk_fwd_varlen are the same functions under shorter names):
   kda_segids_to_cu_seqlens(segment_ids, max_segs) -> (cu_seqlens, n_segs)
   kda_short_conv_varlen(x, weight, segment_ids=None) -> y
   kda_chunk_fwd_varlen(q, k, v, g, beta, segment_ids=None, scale=1.0) -> o
+  kda_chunk_plan_varlen / kda_chunk_fwd_varlen(..., planned=True), the same in two calls
+  kda_chunk_fwd_varlen_state(...) -> (o, final states): per-segment initial/final state
+  kda_chunk_bwd_varlen(...) -> (dq, dk, dv, dg, dbeta), and kda_varlen (autograd)
+The forward wrappers read the kernels' device status word after the call and
+raise KdaDeviceError when a bit is set, unless told not to (check=False) or
+given a status tensor of the caller's.
 """
 from __future__ import annotations
 
@@ -394,7 +401,13 @@ def kda_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tenso
     return _KdaVarlen.apply(q, k, v, g, beta, segment_ids, scale, B, T)
 
 
-__all__ = ["kda_segids_to_cu_seqlens", "kda_short_conv_varlen", "kda_chunk_fwd_varlen",
+# The shorter names the boundary's description uses, for the same calls.
+segids_to_cu_seqlens = kda_segids_to_cu_seqlens
+short_conv_varlen = kda_short_conv_varlen
+chunk_fwd_varlen = kda_chunk_fwd_varlen
+
+__all__ = ["segids_to_cu_seqlens", "short_conv_varlen", "chunk_fwd_varlen",
+           "kda_segids_to_cu_seqlens", "kda_short_conv_varlen", "kda_chunk_fwd_varlen",
            "kda_chunk_plan_varlen", "kda_chunk_fwd_varlen_state", "kda_chunk_bwd_varlen", "kda_varlen",
            "chunk_fwd_workspace_bytes", "load_library", "header_functions", "KdaError",
            "KdaDeviceError", "KDA_DEV_DECAY_RANGE", "KDA_DEV_TIMEOUT"]

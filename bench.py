@@ -556,6 +556,7 @@ def run_gb300(args):
     # else the eager call (planner + kernel)
     dom_ms = kernel_ms if kernel_ms is not None else chunk_ms
     achieved = bytes_launch / (dom_ms / 1e3) / 1e9
+    tc_path = wl.dtype == torch.bfloat16 and wl.d_qk == 128
     line = {
         "metric": METRIC,
         "value": value,
@@ -587,8 +588,8 @@ def run_gb300(args):
                    "parallelism": f"replicas x{ws} (rows independent)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": chunk_traffic(wl),
-                     "kernel": (("tc::chunk_kernel" if wl.dtype == torch.bfloat16 and
-                                 wl.d_qk == 128 else "the token-recurrence kernels") +
+                     "kernel": (("tc::chunk_kernel (state-only pass, fast and safe "
+                                 "instantiations)" if tc_path else "the token-recurrence kernels") +
                                 " (kda_chunk_fwd_varlen_planned), timed by events in the graph, "
                                 f"mean of the last {len(pairs)} timed steps"
                                 if kernel_ms is not None else
@@ -612,7 +613,11 @@ def run_gb300(args):
             if ms_ is not None
         },
         "real_tokens_per_s": real_tokens * ws / (ms / 1e3),
-        "gpu_launches": args.steps * (7 if seg is not None else 6),
+        # per step: the scan (with ids), 3 convs, 2 planner kernels and the forward's three
+        # chunk kernels (state-only pass, fast, safe; the first and last exit at once when
+        # nothing is split or out of range); the token-recurrence path launches one forward
+        "gpu_launches": args.steps * ((9 if tc_path else 7) if seg is not None else
+                                      (8 if tc_path else 6)),
         "clocks": clk,
         "e2e": e2e,
     }

@@ -111,10 +111,19 @@ kda_status_t kda_short_conv_varlen(const void *x, const void *weight,
 
 /*
  * kda_chunk_fwd_varlen_workspace_size -- bytes of device scratch that
- * kda_chunk_fwd_varlen needs for these sizes (0 on invalid sizes).
+ * kda_chunk_fwd_varlen uses for these sizes (0 on invalid sizes): the minimum
+ * below, plus, for bf16 with 128-wide heads, room for the states that let it
+ * split long segments (one 64 KB state per head per 64 chunks; see
+ * kda_chunk_fwd_varlen).
+ *
+ * kda_chunk_fwd_varlen_workspace_min -- the least scratch the forward entry
+ * points accept. With less than the full size they split fewer long segments,
+ * or none; the results are the same to rounding.
  */
 size_t kda_chunk_fwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int32_t d_qk,
                                            int32_t d_v, kda_dtype_t dtype);
+size_t kda_chunk_fwd_varlen_workspace_min(int64_t B, int64_t T, int32_t H, int32_t d_qk,
+                                          int32_t d_v, kda_dtype_t dtype);
 
 /*
  * kda_chunk_fwd_varlen -- the KDA recurrence over packed sequences,
@@ -149,9 +158,19 @@ size_t kda_chunk_fwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int3
  * unreliable. (fp32 inputs and 64-wide heads run the token recurrence, which
  * has no such limit.)
  *
+ * Long segments: the state is serial along a segment, so one long document
+ * would keep a single multiprocessor busy while the others finish. When the
+ * workspace has room, a segment longer than one multiprocessor's share of the
+ * work (chunks x heads / multiprocessors) by more than 32 chunks is cut into
+ * pieces. A state-only pass computes, in parallel, each leading piece's end
+ * state from a zero start, and hands each piece's start state to the next one
+ * along the segment; the forward then runs every piece from its start state.
+ *
  *   workspace        device scratch of at least
- *                    kda_chunk_fwd_varlen_workspace_size(...) bytes, 256-byte
+ *                    kda_chunk_fwd_varlen_workspace_min(...) bytes, and best
+ *                    kda_chunk_fwd_varlen_workspace_size(...), 256-byte
  *                    aligned; its contents on entry do not matter.
+ *   workspace_bytes  its size, which bounds how many segments are split.
  *   status_dev       device uint32 or NULL; bits are ORed in, never cleared.
  *
  * Returns KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE
@@ -182,10 +201,12 @@ kda_status_t kda_chunk_fwd_varlen(const void *q, const void *k, const void *v, c
  *                            takes kda_chunk_fwd_varlen's arguments. Its
  *                            workspace must hold a plan of the same
  *                            segment_ids contents, B, T, H, d_qk, d_v and
- *                            dtype, complete or ordered before the call
- *                            (same stream, or an event). A plan serves any
- *                            number of planned calls, one at a time, until
- *                            another call writes the workspace.
+ *                            dtype, and the same workspace_bytes (which
+ *                            fix how long segments are split), complete or
+ *                            ordered before the call (same stream, or an
+ *                            event). A plan serves any number of planned
+ *                            calls, one at a time, until another call
+ *                            writes the workspace.
  *
  * Paths that plan inside the forward (dtype KDA_F32, or 64-wide heads) have
  * nothing to plan ahead: kda_chunk_plan_varlen only checks its arguments and

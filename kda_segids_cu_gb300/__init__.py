@@ -76,6 +76,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.kda_short_conv_varlen.restype = ctypes.c_int
     lib.kda_chunk_fwd_varlen_workspace_size.argtypes = [i64, i64, i32, i32, i32, ctypes.c_int]
     lib.kda_chunk_fwd_varlen_workspace_size.restype = ctypes.c_size_t
+    lib.kda_chunk_fwd_varlen_workspace_min.argtypes = [i64, i64, i32, i32, i32, ctypes.c_int]
+    lib.kda_chunk_fwd_varlen_workspace_min.restype = ctypes.c_size_t
     lib.kda_chunk_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32,
                                          ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, vp,
                                          ctypes.c_size_t, u32p, vp]
@@ -204,9 +206,13 @@ def kda_short_conv_varlen(x: torch.Tensor, weight: torch.Tensor,
     return y
 
 
-def chunk_fwd_workspace_bytes(B: int, T: int, H: int, d_qk: int, d_v: int, dtype) -> int:
-    return int(load_library().kda_chunk_fwd_varlen_workspace_size(B, T, H, d_qk, d_v,
-                                                                  _dtype_code(dtype)))
+def chunk_fwd_workspace_bytes(B: int, T: int, H: int, d_qk: int, d_v: int, dtype,
+                              minimum: bool = False) -> int:
+    """Workspace bytes of the forward: the full size (room to split long segments) or, with
+    minimum=True, the least the entry points accept."""
+    lib = load_library()
+    fn = lib.kda_chunk_fwd_varlen_workspace_min if minimum else lib.kda_chunk_fwd_varlen_workspace_size
+    return int(fn(B, T, H, d_qk, d_v, _dtype_code(dtype)))
 
 
 def _chunk_args(q, k, v, g, beta, segment_ids, B, T, out, workspace, out_dtype,

@@ -4,7 +4,7 @@
 
 namespace kda {
 size_t recurrent_workspace_bytes(int64_t N);
-size_t tc_workspace_bytes(int64_t N, int32_t H);
+size_t tc_workspace_bytes(int64_t N, int32_t H, bool with_slots);
 kda_status_t launch_recurrent(const void* q, const void* k, const void* v, const void* g,
                               const void* beta, const int32_t* seg, int64_t B, int64_t T,
                               int32_t H, int32_t D, float scale, kda_dtype_t dtype,
@@ -15,12 +15,12 @@ kda_status_t launch_recurrent_state(const void* q, const void* k, const void* v,
                                     kda_dtype_t out_dtype, void* o, void* ws, const float* init,
                                     float* fin, int64_t n_state, cudaStream_t stream);
 kda_status_t launch_chunk_plan(const int32_t* seg, int64_t B, int64_t T, int32_t H, int32_t D,
-                               bool with_state, void* ws, cudaStream_t stream);
+                               bool with_state, void* ws, size_t ws_bytes, cudaStream_t stream);
 kda_status_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* g,
                              const void* beta, const int32_t* seg, int64_t B, int64_t T,
                              int32_t H, int32_t D, float scale, kda_dtype_t out_dtype, void* o,
-                             void* ws, uint32_t* status_dev, const float* init, float* fin,
-                             int64_t n_state, bool plan, cudaStream_t stream);
+                             void* ws, size_t ws_bytes, uint32_t* status_dev, const float* init,
+                             float* fin, int64_t n_state, bool plan, cudaStream_t stream);
 size_t bwd_workspace_bytes(int64_t N, int32_t H, int32_t D);
 kda_status_t launch_bwd(const void* q, const void* k, const void* v, const void* g,
                         const void* beta, const void* d_o, const int32_t* seg, int64_t B,
@@ -107,14 +107,26 @@ kda_status_t kda_short_conv_varlen(const void* x, const void* weight,
                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
-size_t kda_chunk_fwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int32_t d_qk,
-                                           int32_t d_v, kda_dtype_t dtype) {
+namespace {
+size_t fwd_workspace(int64_t B, int64_t T, int32_t H, int32_t d_qk, int32_t d_v,
+                     kda_dtype_t dtype, bool with_slots) {
     if (!token_count_ok(B, T) || H < 1 || d_qk < 1 || d_v < 1 || !valid_dtype(dtype)) return 0;
     const int64_t N = B * T;
     const size_t rec = kda::recurrent_workspace_bytes(N);
     if (dtype != KDA_BF16) return rec;
-    const size_t tc = kda::tc_workspace_bytes(N, H);
+    const size_t tc = kda::tc_workspace_bytes(N, H, with_slots && d_qk == 128 && d_v == 128);
     return tc > rec ? tc : rec;
+}
+}  // namespace
+
+size_t kda_chunk_fwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int32_t d_qk,
+                                           int32_t d_v, kda_dtype_t dtype) {
+    return fwd_workspace(B, T, H, d_qk, d_v, dtype, true);
+}
+
+size_t kda_chunk_fwd_varlen_workspace_min(int64_t B, int64_t T, int32_t H, int32_t d_qk,
+                                          int32_t d_v, kda_dtype_t dtype) {
+    return fwd_workspace(B, T, H, d_qk, d_v, dtype, false);
 }
 
 
@@ -129,7 +141,7 @@ kda_status_t check_fwd_args(const void* q, const void* k, const void* v, const v
     const kda_status_t s = kda::check_fwd_inputs(q, k, v, g, beta, segment_ids, B, T, H, d_qk,
                                                  d_v, dtype, out_dtype, o, status_dev);
     if (s != KDA_OK) return s;
-    const size_t need = kda_chunk_fwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
+    const size_t need = kda_chunk_fwd_varlen_workspace_min(B, T, H, d_qk, d_v, dtype);
     if (!workspace || workspace_bytes < need || !kda::aligned(workspace, 256))
         return KDA_ERR_WORKSPACE;
     return KDA_OK;
@@ -147,8 +159,8 @@ kda_status_t chunk_fwd(const void* q, const void* k, const void* v, const void* 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == KDA_BF16)
         return kda::launch_chunk_tc(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale,
-                                    out_dtype, o, workspace, status_dev, nullptr, nullptr, 0,
-                                    plan, st);
+                                    out_dtype, o, workspace, workspace_bytes, status_dev, nullptr,
+                                    nullptr, 0, plan, st);
     return kda::launch_recurrent(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale, dtype,
                                  out_dtype, o, workspace, st);
 }
@@ -173,11 +185,11 @@ kda_status_t kda_chunk_plan_varlen(const int32_t* segment_ids, int64_t B, int64_
     if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return KDA_ERR_UNSUPPORTED;
     if (int64_t(H) * d_qk > 65536) return KDA_ERR_UNSUPPORTED;
     if (segment_ids && !kda::aligned(segment_ids, 4)) return KDA_ERR_INVALID_ARG;
-    const size_t need = kda_chunk_fwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
+    const size_t need = kda_chunk_fwd_varlen_workspace_min(B, T, H, d_qk, d_v, dtype);
     if (!workspace || workspace_bytes < need || !kda::aligned(workspace, 256))
         return KDA_ERR_WORKSPACE;
     if (dtype != KDA_BF16) return KDA_OK;     // the fp32 path plans inside its call
-    return kda::launch_chunk_plan(segment_ids, B, T, H, d_qk, false, workspace,
+    return kda::launch_chunk_plan(segment_ids, B, T, H, d_qk, false, workspace, workspace_bytes,
                                   reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -216,14 +228,14 @@ kda_status_t kda_chunk_fwd_varlen_state(const void* q, const void* k, const void
         return KDA_ERR_INVALID_ARG;
     if (segment_ids && !kda::aligned(segment_ids, 4)) return KDA_ERR_INVALID_ARG;
     if (status_dev && !kda::aligned(status_dev, 4)) return KDA_ERR_INVALID_ARG;
-    const size_t need = kda_chunk_fwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
+    const size_t need = kda_chunk_fwd_varlen_workspace_min(B, T, H, d_qk, d_v, dtype);
     if (!workspace || workspace_bytes < need || !kda::aligned(workspace, 256))
         return KDA_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == KDA_BF16 && d_qk == 128)   // tensor-core chunked form, then the state pass
         return kda::launch_chunk_tc(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale,
-                                    out_dtype, o, workspace, status_dev, initial_state,
-                                    final_state, n_state, true, st);
+                                    out_dtype, o, workspace, workspace_bytes, status_dev,
+                                    initial_state, final_state, n_state, true, st);
     return kda::launch_recurrent_state(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale, dtype,
                                        out_dtype, o, workspace, initial_state, final_state,
                                        n_state, st);

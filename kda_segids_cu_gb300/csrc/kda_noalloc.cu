@@ -64,7 +64,7 @@ extern "C" kda_status_t kda_chunk_fwd_varlen_noalloc(
     const kda_status_t chk = kda::check_fwd_inputs(q, k, v, g, beta, segment_ids, B, T, H, d_qk,
                                                    d_v, dtype, out_dtype, o, status_dev);
     if (chk != KDA_OK) return chk;
-    const size_t need = kda_chunk_fwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
+    const size_t need = kda_chunk_fwd_varlen_workspace_min(B, T, H, d_qk, d_v, dtype);
     if (need == 0) return KDA_ERR_INVALID_ARG;
     if (need > size_t(KDA_NOALLOC_SCRATCH_BYTES)) return KDA_ERR_WORKSPACE;
     void* scratch = nullptr;

@@ -34,6 +34,16 @@ def test_workspace_size_host_logic(lib):
     assert f(1, 8, 0, 64, 64, kda.KDA_F32) == 0
     assert f(1 << 20, 1 << 12, 1, 64, 64, kda.KDA_F32) == 0   # B*T >= 2^31
     assert f(1, 8, 1, 64, 64, 7) == 0                     # unknown dtype
+    # the minimum is the plan (or the token recurrence's list); the full size adds one 64 KB
+    # state per head per 64 chunks for splitting long segments (bf16, 128-wide heads only)
+    m = lib.kda_chunk_fwd_varlen_workspace_min
+    for (B, T, H) in ((4, 8192, 16), (1, 131072, 32), (2, 100, 3)):
+        n_chunks = (B * T + 63) // 64
+        full, least = f(B, T, H, 128, 128, kda.KDA_BF16), m(B, T, H, 128, 128, kda.KDA_BF16)
+        assert full >= least and full >= -(-n_chunks // 64) * H * 128 * 128 * 4
+        assert m(B, T, H, 64, 64, kda.KDA_BF16) == f(B, T, H, 64, 64, kda.KDA_BF16)
+        assert m(B, T, H, 64, 64, kda.KDA_F32) == f(B, T, H, 64, 64, kda.KDA_F32) == 8 * B * T + 256
+    assert m(0, 8, 1, 64, 64, kda.KDA_F32) == 0
 
 
 FAKE = ctypes.c_void_p(4096)    # aligned, never dereferenced: validation fails first
@@ -64,7 +74,7 @@ def test_conv_rejects_invalid_arguments(lib):
 @pytest.mark.parametrize("fname", ["kda_chunk_fwd_varlen", "kda_chunk_fwd_varlen_planned"])
 def test_chunk_rejects_invalid_arguments(lib, fname):
     f = getattr(lib, fname)
-    ws = lib.kda_chunk_fwd_varlen_workspace_size(1, 64, 2, 64, 64, kda.KDA_BF16)
+    ws = lib.kda_chunk_fwd_varlen_workspace_min(1, 64, 2, 64, 64, kda.KDA_BF16)
     args = [FAKE] * 5 + [None, 1, 64, 2, 64, 64, ctypes.c_float(1.0), kda.KDA_BF16, kda.KDA_BF16,
                          FAKE, FAKE, ws, None, None]
 
@@ -93,7 +103,7 @@ def test_chunk_rejects_invalid_arguments(lib, fname):
 
 def test_chunk_plan_rejects_invalid_arguments(lib):
     f = lib.kda_chunk_plan_varlen
-    ws = lib.kda_chunk_fwd_varlen_workspace_size(1, 64, 2, 128, 128, kda.KDA_BF16)
+    ws = lib.kda_chunk_fwd_varlen_workspace_min(1, 64, 2, 128, 128, kda.KDA_BF16)
     args = [FAKE, 1, 64, 2, 128, 128, kda.KDA_BF16, FAKE, ws, None]
 
     def call(**over):
@@ -118,7 +128,7 @@ def test_chunk_plan_rejects_invalid_arguments(lib):
 
 def test_chunk_state_rejects_invalid_arguments(lib):
     f = lib.kda_chunk_fwd_varlen_state
-    ws = lib.kda_chunk_fwd_varlen_workspace_size(1, 64, 2, 64, 64, kda.KDA_BF16)
+    ws = lib.kda_chunk_fwd_varlen_workspace_min(1, 64, 2, 64, 64, kda.KDA_BF16)
     args = [FAKE] * 5 + [None, 1, 64, 2, 64, 64, ctypes.c_float(1.0), kda.KDA_BF16, kda.KDA_BF16,
                          FAKE, FAKE, FAKE, 3, FAKE, ws, None, None]
 

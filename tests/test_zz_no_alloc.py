@@ -85,16 +85,17 @@ def test_noalloc_matches_allocating_entry_point(dtype, D):
 
 
 def test_noalloc_size_limit_on_the_host():
-    """The array's size bounds the problem: the workspace of MAX_TOKENS tokens fits it
-    and one token more does not, for either dtype and head width (no launch)."""
+    """The array's size bounds the problem: the least workspace of MAX_TOKENS tokens fits it
+    and one token more does not, for either dtype and head width (no launch). A problem
+    that fits uses whatever room is left for splitting long segments."""
     lib = kda.load_library()
     for dt, D in ((kda.KDA_BF16, 128), (kda.KDA_BF16, 64), (kda.KDA_F32, 64)):
         for H in (1, 16, 64):
-            assert lib.kda_chunk_fwd_varlen_workspace_size(1, MAX_TOKENS, H, D, D, dt) <= \
+            assert lib.kda_chunk_fwd_varlen_workspace_min(1, MAX_TOKENS, H, D, D, dt) <= \
                 SCRATCH_BYTES
-            assert lib.kda_chunk_fwd_varlen_workspace_size(1, MAX_TOKENS + 1, H, D, D, dt) > \
+            assert lib.kda_chunk_fwd_varlen_workspace_min(1, MAX_TOKENS + 1, H, D, D, dt) > \
                 SCRATCH_BYTES
-            assert lib.kda_chunk_fwd_varlen_workspace_size(4, MAX_TOKENS // 4, H, D, D, dt) <= \
+            assert lib.kda_chunk_fwd_varlen_workspace_min(4, MAX_TOKENS // 4, H, D, D, dt) <= \
                 SCRATCH_BYTES
 
 

@@ -18,9 +18,8 @@ struct Plan {                      // device view of the workspace
                                    // finished (the last one rewinds [1] and [5]), [6] units
                                    // the fast chunk kernel left to the safe one, [7] split
                                    // pieces with a successor (= slots used), [8] the state-only
-                                   // pass's next item, [9] its CTAs finished, [10] its call
-                                   // count (the epoch of the slots' flags), [11] slots the
-                                   // workspace holds
+                                   // phase's next item, [10] the fast kernel's call count (the
+                                   // epoch of the slots' flags), [11] slots the workspace holds
     ChunkMeta* meta;               // [n_chunks]
     int32_t* first_cut;            // [n_chunks] first start-or-padding row, 64 if none
     int32_t* block_cut;            // [n_blocks]

@@ -588,8 +588,8 @@ def run_gb300(args):
                    "parallelism": f"replicas x{ws} (rows independent)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": chunk_traffic(wl),
-                     "kernel": (("tc::chunk_kernel (state-only pass, fast and safe "
-                                 "instantiations)" if tc_path else "the token-recurrence kernels") +
+                     "kernel": (("tc::chunk_kernel (fast and safe instantiations)" if tc_path
+                                 else "the token-recurrence kernels") +
                                 " (kda_chunk_fwd_varlen_planned), timed by events in the graph, "
                                 f"mean of the last {len(pairs)} timed steps"
                                 if kernel_ms is not None else
@@ -613,11 +613,11 @@ def run_gb300(args):
             if ms_ is not None
         },
         "real_tokens_per_s": real_tokens * ws / (ms / 1e3),
-        # per step: the scan (with ids), 3 convs, 2 planner kernels and the forward's three
-        # chunk kernels (state-only pass, fast, safe; the first and last exit at once when
-        # nothing is split or out of range); the token-recurrence path launches one forward
-        "gpu_launches": args.steps * ((9 if tc_path else 7) if seg is not None else
-                                      (8 if tc_path else 6)),
+        # per step: the scan (with ids), 3 convs, 2 planner kernels and the forward's two
+        # chunk kernels (fast, then safe, which exits at once when nothing is out of range or
+        # split); the token-recurrence path launches one forward kernel
+        "gpu_launches": args.steps * ((8 if tc_path else 7) if seg is not None else
+                                      (7 if tc_path else 6)),
         "clocks": clk,
         "e2e": e2e,
     }

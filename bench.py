@@ -19,6 +19,7 @@ independent, no collective on the data path): weak scaling.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -259,11 +260,13 @@ class ClockSampler:
 
 
 def make_step_inputs(wl: synth.Workload, device):
+    """The forward's inputs and the three convs' (x and weights seeded apart), all masked by
+    the forward's segment ids, as in one attention layer."""
     kin = synth.make_kda_inputs(wl, device=device)
-    cq = synth.make_conv_inputs(wl, seed=synth.default_seed(wl.name) + 101, device=device)
-    ck = synth.make_conv_inputs(wl, seed=synth.default_seed(wl.name) + 102, device=device)
-    cv = synth.make_conv_inputs(wl, seed=synth.default_seed(wl.name) + 103, device=device)
-    return kin, [cq, ck, cv]
+    convs = [dataclasses.replace(
+        synth.make_conv_inputs(wl, seed=synth.default_seed(wl.name) + 101 + i, device=device),
+        segment_ids=kin.segment_ids) for i in range(3)]
+    return kin, convs
 
 
 def run_gb300(args):
@@ -417,6 +420,53 @@ def run_gb300(args):
     real_tokens = int((seg != 0).sum().item()) if seg is not None else N
     if int(status.item()) != 0:       # outputs of the timed calls are unreliable: no number
         raise RuntimeError(f"device status {int(status.item()):#x} after the timed steps")
+
+    # ---- the step with the convs fused into the chunk kernel (kda_chunk_fwd_varlen_conv),
+    # timed apart: the same graph shape (scan and plan on the side stream), K replays ----
+    fused = None
+    if wl.dtype == torch.bfloat16 and wl.d_qk == 128 and wl.k_conv <= 4:
+        o_f = torch.empty_like(o)
+
+        def fused_step():
+            cur = torch.cuda.current_stream()
+            fork = torch.cuda.Event()
+            fork.record(cur)
+            side.wait_event(fork)
+            with torch.cuda.stream(side):
+                if seg is not None:
+                    kda.kda_segids_to_cu_seqlens(seg, wl.max_segs, out=cu, n_segs_out=nseg)
+                kda.kda_chunk_plan_varlen(seg, wl.B, wl.T, H, wl.d_qk, wl.d_v, wl.dtype, work)
+            join = torch.cuda.Event()
+            join.record(side)
+            cur.wait_event(join)
+            kda.kda_chunk_fwd_varlen_conv(*(c.x for c in convs), *(c.w for c in convs), kin.g,
+                                          kin.beta, seg, B=wl.B, T=wl.T, out=o_f,
+                                          workspace=work, status=status, planned=True)
+
+        g_f = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_f):
+            fused_step()
+        for _ in range(max(3, args.warmup)):
+            g_f.replay()
+        torch.cuda.synchronize()
+        fa = torch.cuda.Event(enable_timing=True)
+        fb = torch.cuda.Event(enable_timing=True)
+        fa.record(stream)
+        for _ in range(args.steps):
+            g_f.replay()
+        fb.record(stream)
+        torch.cuda.synchronize()
+        fused_ms = fa.elapsed_time(fb) / args.steps
+        # the unfused forward on the last step's conv outputs, for the comparison
+        o_u = kda.kda_chunk_fwd_varlen(qkv[0], qkv[1], qkv[2], kin.g, kin.beta, seg, B=wl.B,
+                                       T=wl.T, workspace=work, status=status, planned=True)
+        torch.cuda.synchronize()
+        fused = {"ms_per_step": fused_ms, "value": N / (fused_ms / 1e3),
+                 "vs_unfused_step": ms_local / fused_ms,
+                 "equal_to_unfused": bool(torch.equal(o_f, o_u)),
+                 "step": "segids->cu_seqlens and the chunk plan (side stream) + "
+                         "kda_chunk_fwd_varlen_conv (the 3 masked convs inside the chunk kernel)"}
+        del o_f, o_u
 
     # ---- per-segment state in and out (kda_chunk_fwd_varlen_state), timed apart ----
     n_state = int(nseg.item()) if seg is not None else wl.B
@@ -613,6 +663,7 @@ def run_gb300(args):
             if ms_ is not None
         },
         "real_tokens_per_s": real_tokens * ws / (ms / 1e3),
+        "fused_conv_step": fused,
         # per step: the scan (with ids), 3 convs, 2 planner kernels and the forward's two
         # chunk kernels (fast, then safe, which exits at once when nothing is out of range or
         # split); the token-recurrence path launches one forward kernel

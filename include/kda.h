@@ -227,6 +227,43 @@ kda_status_t kda_chunk_fwd_varlen_planned(const void *q, const void *k, const vo
                                           uint32_t *status_dev, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd_varlen_conv -- kda_chunk_fwd_varlen with the three
+ * segment-masked short convolutions that produce q, k and v ([RFC-0025] 方案 §3
+ * "ShortConvolution segment 边界 mask") done inside the chunk kernel: the
+ * prologue fusion that [RFC-0026] §3.3's kernel wrapper implies. The result is
+ *     q = conv(x_q, w_q), k = conv(x_k, w_k), v = conv(x_v, w_v)   (each as
+ *     kda_short_conv_varlen with these segment_ids, rounded to dtype)
+ *     o = kda_chunk_fwd_varlen(q, k, v, g, beta, ...)
+ * equal to those four calls bit for bit, but q, k and v are never written to
+ * device memory: the kernel reads x_q, x_k and x_v (plus the k_conv - 1 tokens
+ * before each 64-token chunk) and convolves them in shared memory. No L2
+ * normalisation of q and k is applied (the pages give no epsilon for it).
+ *
+ *   x_q, x_k, x_v  device [B*T, H*d_qk] of `dtype` (the convs' inputs, laid out
+ *                  like q, k, v); none may overlap o.
+ *   w_q, w_k, w_v  device [k_conv, H*d_qk] of `dtype`, 16-byte aligned: tap j
+ *                  weighs the token j steps back, as in kda_short_conv_varlen.
+ *   k_conv         1..4.
+ *   planned        0: plan inside the call, as kda_chunk_fwd_varlen; 1: the
+ *                  workspace holds the plan of kda_chunk_plan_varlen, under the
+ *                  rules of kda_chunk_fwd_varlen_planned.
+ *
+ * The other arguments are kda_chunk_fwd_varlen's, with the same workspace
+ * sizes (long segments are split the same way). Supported: dtype KDA_BF16 with
+ * d_qk == d_v == 128; other dtypes, widths or k_conv return
+ * KDA_ERR_UNSUPPORTED (run the convs, then kda_chunk_fwd_varlen). Returns as
+ * kda_chunk_fwd_varlen. Calls that share a workspace must not overlap in time.
+ */
+kda_status_t kda_chunk_fwd_varlen_conv(const void *x_q, const void *x_k, const void *x_v,
+                                       const void *w_q, const void *w_k, const void *w_v,
+                                       int32_t k_conv, const void *g, const void *beta,
+                                       const int32_t *segment_ids, int64_t B, int64_t T,
+                                       int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                       kda_dtype_t dtype, kda_dtype_t out_dtype, void *o,
+                                       void *workspace, size_t workspace_bytes, int planned,
+                                       uint32_t *status_dev, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_varlen_state -- kda_chunk_fwd_varlen with per-segment recurrent
  * state in and out: the initial_state and output_final_state kwargs that
  * [RFC-0026] passes to the chunked KDA call, one state per packed sequence.

@@ -87,6 +87,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.kda_chunk_plan_varlen.restype = ctypes.c_int
     lib.kda_chunk_fwd_varlen_planned.argtypes = lib.kda_chunk_fwd_varlen.argtypes
     lib.kda_chunk_fwd_varlen_planned.restype = ctypes.c_int
+    lib.kda_chunk_fwd_varlen_conv.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, i64, i64,
+                                              i32, i32, i32, ctypes.c_float, ctypes.c_int,
+                                              ctypes.c_int, vp, vp, ctypes.c_size_t, ctypes.c_int,
+                                              u32p, vp]
+    lib.kda_chunk_fwd_varlen_conv.restype = ctypes.c_int
     lib.kda_chunk_fwd_varlen_state.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32,
                                                ctypes.c_float, ctypes.c_int, ctypes.c_int, vp,
                                                vp, vp, i64, vp, ctypes.c_size_t, u32p, vp]
@@ -294,6 +299,51 @@ def kda_chunk_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: t
     _check(name, fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(seg), B, T, H, Dk, Dv,
                     float(scale), dt, odt, _ptr(o), _ptr(workspace), workspace.numel(),
                     _ptr(status), _stream_ptr(st)))
+    if check:
+        _raise_on_status(name, status, st)
+    return o
+
+
+def kda_chunk_fwd_varlen_conv(x_q: torch.Tensor, x_k: torch.Tensor, x_v: torch.Tensor,
+                              w_q: torch.Tensor, w_k: torch.Tensor, w_v: torch.Tensor,
+                              g: torch.Tensor, beta: torch.Tensor,
+                              segment_ids: torch.Tensor | None = None, scale: float = 1.0,
+                              B: int | None = None, T: int | None = None, stream=None,
+                              out: torch.Tensor | None = None,
+                              workspace: torch.Tensor | None = None,
+                              status: torch.Tensor | None = None,
+                              out_dtype: torch.dtype | None = None, planned: bool = False,
+                              check: bool | None = None) -> torch.Tensor:
+    """kda_chunk_fwd_varlen on q, k, v = the segment-masked short convs of x_q, x_k, x_v
+    (weights w_q, w_k, w_v [K, H*D], as kda_short_conv_varlen), with the convs done inside
+    the chunk kernel. The result equals the three conv calls followed by
+    kda_chunk_fwd_varlen bit for bit. x_*: [B, T, H*D] or shaped like g. bf16, 128-wide
+    heads and K <= 4; other arguments as in kda_chunk_fwd_varlen."""
+    if planned and workspace is None:
+        raise ValueError("planned=True needs the workspace that holds the plan")
+    g = _dev(g, "g")
+    xs = []
+    for x, n in ((x_q, "x_q"), (x_k, "x_k"), (x_v, "x_v")):
+        x = _dev(x, n)
+        if x.numel() != g.numel():
+            raise ValueError(f"{n} must hold as many values as g")
+        xs.append(x.view(g.shape))
+    ws_ = []
+    for w, n in ((w_q, "w_q"), (w_k, "w_k"), (w_v, "w_v")):
+        w = _dev(w, n)
+        if w.dim() != 2 or w.shape[1] != g.shape[-2] * g.shape[-1] or w.dtype != g.dtype:
+            raise ValueError(f"{n} must be [K, H*D] of g's dtype")
+        ws_.append(w)
+    if not (ws_[0].shape == ws_[1].shape == ws_[2].shape):
+        raise ValueError("the three conv weights must have one shape")
+    q, k, v, g, beta, seg, B, T, H, Dk, Dv, dt, odt, o, workspace = _chunk_args(
+        xs[0], xs[1], xs[2], g, beta, segment_ids, B, T, out, workspace, out_dtype)
+    status, check, st = _status_word(status, check, q.device, stream)
+    name = "kda_chunk_fwd_varlen_conv"
+    _check(name, load_library().kda_chunk_fwd_varlen_conv(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(ws_[0]), _ptr(ws_[1]), _ptr(ws_[2]), ws_[0].shape[0],
+        _ptr(g), _ptr(beta), _ptr(seg), B, T, H, Dk, Dv, float(scale), dt, odt, _ptr(o),
+        _ptr(workspace), workspace.numel(), int(planned), _ptr(status), _stream_ptr(st)))
     if check:
         _raise_on_status(name, status, st)
     return o

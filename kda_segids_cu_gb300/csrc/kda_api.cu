@@ -20,7 +20,8 @@ kda_status_t launch_chunk_tc(const void* q, const void* k, const void* v, const 
                              const void* beta, const int32_t* seg, int64_t B, int64_t T,
                              int32_t H, int32_t D, float scale, kda_dtype_t out_dtype, void* o,
                              void* ws, size_t ws_bytes, uint32_t* status_dev, const float* init,
-                             float* fin, int64_t n_state, bool plan, cudaStream_t stream);
+                             float* fin, int64_t n_state, bool plan, cudaStream_t stream,
+                             const ConvIn* conv = nullptr);
 size_t bwd_workspace_bytes(int64_t N, int32_t H, int32_t D);
 kda_status_t launch_bwd(const void* q, const void* k, const void* v, const void* g,
                         const void* beta, const void* d_o, const int32_t* seg, int64_t B,
@@ -202,6 +203,30 @@ kda_status_t kda_chunk_fwd_varlen_planned(const void* q, const void* k, const vo
                                           uint32_t* status_dev, kda_stream_t stream) {
     return chunk_fwd(q, k, v, g, beta, segment_ids, B, T, H, d_qk, d_v, scale, dtype, out_dtype,
                      o, workspace, workspace_bytes, status_dev, false, stream);
+}
+
+kda_status_t kda_chunk_fwd_varlen_conv(const void* x_q, const void* x_k, const void* x_v,
+                                       const void* w_q, const void* w_k, const void* w_v,
+                                       int32_t k_conv, const void* g, const void* beta,
+                                       const int32_t* segment_ids, int64_t B, int64_t T,
+                                       int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                       kda_dtype_t dtype, kda_dtype_t out_dtype, void* o,
+                                       void* workspace, size_t workspace_bytes, int planned,
+                                       uint32_t* status_dev, kda_stream_t stream) {
+    if (!w_q || !w_k || !w_v) return KDA_ERR_INVALID_ARG;
+    const kda_status_t chk = check_fwd_args(x_q, x_k, x_v, g, beta, segment_ids, B, T, H, d_qk,
+                                            d_v, dtype, out_dtype, o, workspace, workspace_bytes,
+                                            status_dev);
+    if (chk != KDA_OK) return chk;
+    if (!kda::aligned(w_q, 16) || !kda::aligned(w_k, 16) || !kda::aligned(w_v, 16))
+        return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 || d_qk != 128 || d_v != 128) return KDA_ERR_UNSUPPORTED;
+    if (k_conv < 1 || k_conv > 4) return KDA_ERR_UNSUPPORTED;
+    const kda::ConvIn conv = {{w_q, w_k, w_v}, k_conv};
+    return kda::launch_chunk_tc(x_q, x_k, x_v, g, beta, segment_ids, B, T, H, d_qk, scale,
+                                out_dtype, o, workspace, workspace_bytes, status_dev, nullptr,
+                                nullptr, 0, planned == 0, reinterpret_cast<cudaStream_t>(stream),
+                                &conv);
 }
 
 kda_status_t kda_chunk_fwd_varlen_state(const void* q, const void* k, const void* v,

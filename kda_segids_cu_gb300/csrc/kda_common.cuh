@@ -84,6 +84,13 @@ struct RowStartTest {
     }
 };
 
+// The short conv fused into the chunked forward: the weights ([k_conv, H*D], the forward's
+// dtype) of the convs that produce q, k and v, and the conv width.
+struct ConvIn {
+    const void* w[3];
+    int32_t k_conv;
+};
+
 // A token starts a segment when it is real (id != 0) and is the first token
 // of its row or its id differs from the previous token's ([RFC-0026] §3.1.1).
 // With no ids, each row is one segment: only row starts are starts.

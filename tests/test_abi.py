@@ -101,6 +101,42 @@ def test_chunk_rejects_invalid_arguments(lib, fname):
     assert call(status=ODD) == -1
 
 
+def test_chunk_conv_rejects_invalid_arguments(lib):
+    """kda_chunk_fwd_varlen_conv: the forward's checks, then its own (no launch is reached)."""
+    f = lib.kda_chunk_fwd_varlen_conv
+    ws = lib.kda_chunk_fwd_varlen_workspace_min(1, 64, 2, 128, 128, kda.KDA_BF16)
+    args = [FAKE] * 6 + [4, FAKE, FAKE, None, 1, 64, 2, 128, 128, ctypes.c_float(1.0),
+                         kda.KDA_BF16, kda.KDA_BF16, FAKE, FAKE, ws, 0, None, None]
+
+    def call(**over):
+        a = list(args)
+        idx = {"xq": 0, "wq": 3, "wv": 5, "K": 6, "g": 7, "seg": 9, "B": 10, "H": 12, "dk": 13,
+               "dv": 14, "dtype": 16, "out_dtype": 17, "o": 18, "ws": 19, "ws_bytes": 20,
+               "status": 22}
+        for k, v in over.items():
+            a[idx[k]] = v
+        return f(*a)
+
+    assert call(xq=None) == -1
+    assert call(wq=None) == -1
+    assert call(wv=ODD) == -1
+    assert call(g=ODD) == -1
+    assert call(o=None) == -1
+    assert call(B=0) == -1
+    assert call(dtype=5) == -1
+    assert call(ws=None) == -4
+    assert call(ws_bytes=ws - 1) == -4
+    # the fused path: bf16, 128-wide heads, up to 4 taps (other forms run the convs apart)
+    assert call(K=0) == -2
+    assert call(K=5) == -2
+    assert call(dtype=kda.KDA_F32, out_dtype=kda.KDA_F32,
+                ws_bytes=lib.kda_chunk_fwd_varlen_workspace_min(1, 64, 2, 128, 128,
+                                                                kda.KDA_F32)) == -2
+    ws64 = lib.kda_chunk_fwd_varlen_workspace_min(1, 64, 2, 64, 64, kda.KDA_BF16)
+    assert call(dk=64, dv=64, ws_bytes=ws64) == -2
+    assert call(dk=96, dv=96) == -2
+
+
 def test_chunk_plan_rejects_invalid_arguments(lib):
     f = lib.kda_chunk_plan_varlen
     ws = lib.kda_chunk_fwd_varlen_workspace_min(1, 64, 2, 128, 128, kda.KDA_BF16)

@@ -386,6 +386,23 @@ kda_status_t kda_chunk_fwd_varlen_noalloc(const void *q, const void *k, const vo
                                           kda_dtype_t dtype, kda_dtype_t out_dtype, void *o,
                                           uint32_t *status_dev, kda_stream_t stream);
 
+/*
+ * kda_selftest_wait_timeout -- a check of the failure detection behind
+ * KDA_DEV_TIMEOUT; not part of the method. The chunk kernels bound every
+ * in-kernel wait by wall time, after which they set KDA_DEV_TIMEOUT and return
+ * with the context intact. This call launches one small kernel that waits,
+ * through the same bounded wait, on a barrier that nothing arrives on, for about
+ * timeout_ns nanoseconds of GPU time, then ORs KDA_DEV_TIMEOUT into *status_dev
+ * and returns. Synchronise, then read the word.
+ *
+ *   timeout_ns   1e6 .. 1e10 (1 ms .. 10 s).
+ *   status_dev   device uint32, 4-byte aligned.
+ *
+ * Returns KDA_OK, KDA_ERR_INVALID_ARG or KDA_ERR_CUDA.
+ */
+kda_status_t kda_selftest_wait_timeout(uint64_t timeout_ns, uint32_t *status_dev,
+                                       kda_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char *kda_status_string(kda_status_t status);
 

@@ -92,6 +92,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                               ctypes.c_int, vp, vp, ctypes.c_size_t, ctypes.c_int,
                                               u32p, vp]
     lib.kda_chunk_fwd_varlen_conv.restype = ctypes.c_int
+    lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_uint64, u32p, vp]
+    lib.kda_selftest_wait_timeout.restype = ctypes.c_int
     lib.kda_chunk_fwd_varlen_state.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32,
                                                ctypes.c_float, ctypes.c_int, ctypes.c_int, vp,
                                                vp, vp, i64, vp, ctypes.c_size_t, u32p, vp]
@@ -347,6 +349,20 @@ def kda_chunk_fwd_varlen_conv(x_q: torch.Tensor, x_k: torch.Tensor, x_v: torch.T
     if check:
         _raise_on_status(name, status, st)
     return o
+
+
+def kda_selftest_wait_timeout(timeout_s: float = 0.05, status: torch.Tensor | None = None,
+                              stream=None) -> torch.Tensor:
+    """Runs the library's bounded in-kernel wait on a barrier that nothing arrives on, for
+    about timeout_s seconds of GPU time; the kernel then sets KDA_DEV_TIMEOUT in `status`
+    (an int32 device word, allocated if None) and returns. Returns the word, unread."""
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    status = _dev(status, "status")
+    _check("kda_selftest_wait_timeout",
+           load_library().kda_selftest_wait_timeout(int(timeout_s * 1e9), _ptr(status),
+                                                    _stream_ptr(stream)))
+    return status
 
 
 def kda_chunk_plan_varlen(segment_ids: torch.Tensor | None, B: int, T: int, H: int, d_qk: int,

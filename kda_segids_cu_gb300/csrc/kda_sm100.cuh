@@ -62,7 +62,8 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Bounded wait: returns false if the phase has not completed after `timeout_ns`
 // nanoseconds of wall time. Each poll may suspend the thread (see mbar_try_wait),
 // so waiting warps take no issue slots from working ones.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                                   uint64_t timeout_ns) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;

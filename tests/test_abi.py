@@ -137,6 +137,15 @@ def test_chunk_conv_rejects_invalid_arguments(lib):
     assert call(dk=96, dv=96) == -2
 
 
+def test_selftest_wait_timeout_rejects_invalid_arguments(lib):
+    """The bounded-wait self-test checks its arguments before any launch."""
+    f = lib.kda_selftest_wait_timeout
+    assert f(50_000_000, None, None) == -1                     # no status word
+    assert f(50_000_000, ODD, None) == -1                      # misaligned
+    assert f(999_999, FAKE, None) == -1                        # below 1 ms
+    assert f(10_000_000_001, FAKE, None) == -1                 # above 10 s
+
+
 def test_chunk_plan_rejects_invalid_arguments(lib):
     f = lib.kda_chunk_plan_varlen
     ws = lib.kda_chunk_fwd_varlen_workspace_min(1, 64, 2, 128, 128, kda.KDA_BF16)

@@ -16,12 +16,17 @@ The arithmetic lives in ``kda_oracle.c`` (plain C, fp64), built with gcc into
                                        final states (RFC-0026's kwargs)
   kda_bwd(q, k, v, g, beta, do, seg)   gradients of kda_fwd, by reverse-mode
                                        differentiation of the recurrence
+  kda_fwd_delta(...)                   the delta-rule update, the reading of the
+                                       method's name (the pages state only the
+                                       additive update)
 
 Parity pins live in tests/test_oracle_*.py. Parity status of each function:
 cu_seqlens, short_conv, kda_fwd and kda_fwd_state are pinned (worked examples
 from the page, library routines, closed forms, brute force and invariants);
 kda_bwd is pinned by finite differences of kda_fwd and by automatic
-differentiation of the brute-force closed form.
+differentiation of the brute-force closed form; kda_fwd_delta by the delta
+rule's defining property (with beta = 1 and unit keys the state reads back v_t
+along k_t exactly), its projector form and its first-token reduction.
 """
 from __future__ import annotations
 
@@ -67,6 +72,8 @@ def _load():
             lib.oracle_kda_fwd.argtypes = [dp, dp, dp, dp, dp, ip, i64, i64, i64, i64, i64,
                                            ctypes.c_double, dp, ctypes.c_int]
             lib.oracle_kda_fwd.restype = ctypes.c_int
+            lib.oracle_kda_fwd_delta.argtypes = lib.oracle_kda_fwd.argtypes
+            lib.oracle_kda_fwd_delta.restype = ctypes.c_int
             lib.oracle_kda_fwd_state.argtypes = [dp, dp, dp, dp, dp, ip, i64, i64, i64, i64, i64,
                                                  ctypes.c_double, dp, dp, i64, dp, ctypes.c_int]
             lib.oracle_kda_fwd_state.restype = ctypes.c_int
@@ -152,6 +159,41 @@ def kda_fwd(q, k, v, g, beta, seg=None, B: int | None = None, T: int | None = No
     o, _ = kda_fwd_state(q, k, v, g, beta, seg, B=B, T=T, scale=scale, n_threads=n_threads,
                          out_dtype=out_dtype)
     return o
+
+
+def kda_fwd_delta(q, k, v, g, beta, seg=None, B: int | None = None, T: int | None = None,
+                  scale: float = 1.0, n_threads: int | None = None,
+                  out_dtype=torch.float64) -> torch.Tensor:
+    """The delta-rule recurrence in fp64: S'_t = S_{t-1} exp(g_t) (key rows), S_t = S'_t +
+    beta_t k_t (v_t - S'_t^T k_t)^T, o_t = scale S_t^T q_t, with kda_fwd's segments and
+    layouts. RFC-0026 names the method Kimi Delta Attention but states only the additive
+    update; this is the reading of that name (the gated delta rule, decay per key channel)."""
+    qa, ka, va, ga = (_np(t, np.float64) for t in (q, k, v, g))
+    ba = _np(beta, np.float64)
+    if seg is not None:
+        sa = _np(seg, np.int32)
+        if sa.ndim == 1:
+            sa = sa[None, :]
+        if B is None:
+            B, T = sa.shape
+        sa = sa.reshape(B, T)
+    else:
+        sa = None
+        if B is None:
+            B, T = 1, qa.reshape(-1, *qa.shape[-2:]).shape[0]
+    Dk, Dv = qa.shape[-1], va.shape[-1]
+    H = qa.shape[-2]
+    N = B * T
+    qa, ka, ga = (a.reshape(N, H, Dk) for a in (qa, ka, ga))
+    va = va.reshape(N, H, Dv)
+    ba = ba.reshape(N, H)
+    o = np.zeros((N, H, Dv), dtype=np.float64)
+    nt = default_threads() if n_threads is None else n_threads
+    rc = _load().oracle_kda_fwd_delta(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), _ptr(ba),
+                                      _ptr(sa), B, T, H, Dk, Dv, float(scale), _ptr(o), int(nt))
+    if rc != 0:
+        raise ValueError("oracle_kda_fwd_delta: bad arguments")
+    return torch.from_numpy(o).to(out_dtype)
 
 
 def kda_fwd_state(q, k, v, g, beta, seg=None, B: int | None = None, T: int | None = None,

@@ -154,10 +154,11 @@ typedef struct {
     const int64_t *units;
     int64_t n_units;
     int64_t next; /* shared counter */
+    int delta;    /* 1: the delta-rule update (oracle_kda_fwd_delta) */
 } kda_job_t;
 
 static void run_unit(const kda_job_t *J, int64_t b, int64_t h, int64_t t0, int64_t t1,
-                     int64_t r, double *S)
+                     int64_t r, double *S, double *W)
 {
     const int64_t H = J->H, Dk = J->Dk, Dv = J->Dv;
     /* the segment's state before its first token: its initial state, or zero */
@@ -174,12 +175,34 @@ static void run_unit(const kda_job_t *J, int64_t b, int64_t h, int64_t t0, int64
         const double *vt = J->v + (p * H + h) * Dv;
         const double bt = J->beta[p * H + h];
         double *ot = J->o + (p * H + h) * Dv;
-        for (int64_t i = 0; i < Dk; ++i) {
-            const double decay = exp(gt[i]);
-            const double bk = bt * kt[i];
-            double *row = S + i * Dv;
-            for (int64_t j = 0; j < Dv; ++j)
-                row[j] = row[j] * decay + bk * vt[j];
+        if (!J->delta) {
+            for (int64_t i = 0; i < Dk; ++i) {
+                const double decay = exp(gt[i]);
+                const double bk = bt * kt[i];
+                double *row = S + i * Dv;
+                for (int64_t j = 0; j < Dv; ++j)
+                    row[j] = row[j] * decay + bk * vt[j];
+            }
+        } else {
+            /* S' = S_{t-1} exp(g_t); u = S'^T k_t; S_t = S' + beta_t k_t (v_t - u)^T */
+            for (int64_t i = 0; i < Dk; ++i) {
+                const double decay = exp(gt[i]);
+                double *row = S + i * Dv;
+                for (int64_t j = 0; j < Dv; ++j)
+                    row[j] *= decay;
+            }
+            for (int64_t j = 0; j < Dv; ++j) {
+                double u = 0.0;
+                for (int64_t i = 0; i < Dk; ++i)
+                    u += S[i * Dv + j] * kt[i];
+                W[j] = vt[j] - u;
+            }
+            for (int64_t i = 0; i < Dk; ++i) {
+                const double bk = bt * kt[i];
+                double *row = S + i * Dv;
+                for (int64_t j = 0; j < Dv; ++j)
+                    row[j] += bk * W[j];
+            }
         }
         for (int64_t j = 0; j < Dv; ++j) {
             double acc = 0.0;
@@ -196,15 +219,16 @@ static void run_unit(const kda_job_t *J, int64_t b, int64_t h, int64_t t0, int64
 static void *kda_worker(void *arg)
 {
     kda_job_t *J = (kda_job_t *)arg;
-    double *S = (double *)malloc(sizeof(double) * (size_t)(J->Dk * J->Dv));
+    double *S = (double *)malloc(sizeof(double) * (size_t)(J->Dk * J->Dv + J->Dv));
     if (!S)
         return NULL;
+    double *W = S + J->Dk * J->Dv;     /* the delta rule's v_t - S'^T k_t */
     for (;;) {
         const int64_t u = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
         if (u >= J->n_units)
             break;
         const int64_t *U = J->units + 5 * u;
-        run_unit(J, U[0], U[1], U[2], U[3], U[4], S);
+        run_unit(J, U[0], U[1], U[2], U[3], U[4], S, W);
     }
     free(S);
     return NULL;
@@ -275,10 +299,10 @@ static int64_t *segment_units(const int32_t *seg, int64_t B, int64_t T, int64_t 
  * is written to fin[r] when fin is given and r < n_state. With init = NULL this
  * is the reset rule above. Returns 0, or -1 on bad arguments.
  */
-int oracle_kda_fwd_state(const double *q, const double *k, const double *v, const double *g,
-                         const double *beta, const int32_t *seg, int64_t B, int64_t T, int64_t H,
-                         int64_t Dk, int64_t Dv, double scale, const double *init, double *fin,
-                         int64_t n_state, double *o, int n_threads)
+static int kda_fwd_run(const double *q, const double *k, const double *v, const double *g,
+                       const double *beta, const int32_t *seg, int64_t B, int64_t T, int64_t H,
+                       int64_t Dk, int64_t Dv, double scale, const double *init, double *fin,
+                       int64_t n_state, double *o, int n_threads, int delta)
 {
     if (!q || !k || !v || !g || !beta || !o || B < 0 || T < 0 || H < 1 || Dk < 1 || Dv < 1 ||
         n_state < 0)
@@ -290,7 +314,7 @@ int oracle_kda_fwd_state(const double *q, const double *k, const double *v, cons
     if (!units)
         return -1;
     kda_job_t J = {q, k, v, g, beta, seg, B, T, H, Dk, Dv, scale, o,
-                   init, fin, n_state, units, n_units, 0};
+                   init, fin, n_state, units, n_units, 0, delta};
     if (n_threads < 1)
         n_threads = 1;
     if (n_threads > 256)
@@ -312,6 +336,15 @@ int oracle_kda_fwd_state(const double *q, const double *k, const double *v, cons
     return 0;
 }
 
+int oracle_kda_fwd_state(const double *q, const double *k, const double *v, const double *g,
+                         const double *beta, const int32_t *seg, int64_t B, int64_t T, int64_t H,
+                         int64_t Dk, int64_t Dv, double scale, const double *init, double *fin,
+                         int64_t n_state, double *o, int n_threads)
+{
+    return kda_fwd_run(q, k, v, g, beta, seg, B, T, H, Dk, Dv, scale, init, fin, n_state, o,
+                       n_threads, 0);
+}
+
 /* The recurrence with every segment starting from zero and no state written. */
 int oracle_kda_fwd(const double *q, const double *k, const double *v, const double *g,
                    const double *beta, const int32_t *seg, int64_t B, int64_t T, int64_t H,
@@ -319,6 +352,25 @@ int oracle_kda_fwd(const double *q, const double *k, const double *v, const doub
 {
     return oracle_kda_fwd_state(q, k, v, g, beta, seg, B, T, H, Dk, Dv, scale, NULL, NULL, 0, o,
                                 n_threads);
+}
+
+/*
+ * The delta rule. [RFC-0026] names the method Kimi Delta Attention, but its
+ * pages state only the additive update above. This is the reading the name
+ * gives: the gated delta rule with a decay per key channel, which writes v_t
+ * against what the decayed state already holds along k_t,
+ *     S'_t = S_{t-1} * exp(g_t)
+ *     S_t  = S'_t + beta_t * k_t (x) (v_t - S'_t^T k_t)
+ *          = (I - beta_t k_t k_t^T) S'_t + beta_t k_t (x) v_t
+ *     o_t  = scale * S_t^T q_t
+ * with the same reset rule and segments. Returns 0, or -1 on bad arguments.
+ */
+int oracle_kda_fwd_delta(const double *q, const double *k, const double *v, const double *g,
+                         const double *beta, const int32_t *seg, int64_t B, int64_t T, int64_t H,
+                         int64_t Dk, int64_t Dv, double scale, double *o, int n_threads)
+{
+    return kda_fwd_run(q, k, v, g, beta, seg, B, T, H, Dk, Dv, scale, NULL, NULL, 0, o,
+                       n_threads, 1);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -30,6 +30,12 @@ MUTATIONS = {
     # per-segment state
     "initial_state_ignored": ("if (J->init && r < J->n_state)", "if (0 && J->init && r < J->n_state)"),
     "state_rank_off_by_one": ("units[5 * n_units + 4] = rank;", "units[5 * n_units + 4] = rank + 1;"),
+    # delta rule
+    "delta_correction_dropped": ("W[j] = vt[j] - u;", "W[j] = vt[j];"),
+    "delta_correction_sign": ("W[j] = vt[j] - u;", "W[j] = vt[j] + u;"),
+    "delta_no_decay": ("                    row[j] *= decay;", "                    row[j] *= 1.0;"),
+    "delta_beta_in_correction": ("u += S[i * Dv + j] * kt[i];", "u += S[i * Dv + j] * bt * kt[i];"),
+    "delta_state_transposed": ("u += S[i * Dv + j] * kt[i];", "u += S[j * Dv + i] * kt[i];"),
     # gradients
     "bwd_no_adjoint_decay": ("                A[i * Dv + j] *= exp(gt[i]);",
                              "                A[i * Dv + j] *= 1.0;"),
@@ -72,6 +78,7 @@ def _pins_pass(monkeypatch, so_path) -> bool:
                                    ctypes.c_double, vp, ctypes.c_int]
     lib.oracle_kda_fwd_state.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                          ctypes.c_double, vp, vp, i64, vp, ctypes.c_int]
+    lib.oracle_kda_fwd_delta.argtypes = lib.oracle_kda_fwd.argtypes
     lib.oracle_kda_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                    ctypes.c_double, vp, vp, vp, vp, vp, vp, ctypes.c_int]
     monkeypatch.setattr(oracle, "_lib", lib)
@@ -80,6 +87,7 @@ def _pins_pass(monkeypatch, so_path) -> bool:
     import tests.test_oracle_kda as tk
     import tests.test_oracle_bwd as tb
     import tests.test_oracle_state as ts
+    import tests.test_oracle_delta as td
     golden = os.path.join(os.path.dirname(tc.__file__), "golden")
     checks = [
         lambda: tc.test_worked_examples(golden),
@@ -99,6 +107,11 @@ def _pins_pass(monkeypatch, so_path) -> bool:
         lambda: ts.test_state_slots_beyond_n_state_and_ranks(),
         lambda: tb.test_finite_differences(),
         lambda: tb.test_autograd_of_closed_form(),
+        lambda: td.test_unit_keys_read_back_their_values(),
+        lambda: td.test_projector_form(),
+        lambda: td.test_first_token_of_a_segment_is_the_additive_rule(),
+        lambda: td.test_zero_beta_writes_nothing_and_linearity_in_v(),
+        lambda: td.test_segments_are_independent(),
     ]
     for c in checks:
         try:

@@ -186,10 +186,10 @@ static void run_unit(const kda_job_t *J, int64_t b, int64_t h, int64_t t0, int64
         } else {
             /* S' = S_{t-1} exp(g_t); u = S'^T k_t; S_t = S' + beta_t k_t (v_t - u)^T */
             for (int64_t i = 0; i < Dk; ++i) {
-                const double decay = exp(gt[i]);
+                const double ei = exp(gt[i]);
                 double *row = S + i * Dv;
                 for (int64_t j = 0; j < Dv; ++j)
-                    row[j] *= decay;
+                    row[j] *= ei;
             }
             for (int64_t j = 0; j < Dv; ++j) {
                 double u = 0.0;
@@ -198,10 +198,10 @@ static void run_unit(const kda_job_t *J, int64_t b, int64_t h, int64_t t0, int64
                 W[j] = vt[j] - u;
             }
             for (int64_t i = 0; i < Dk; ++i) {
-                const double bk = bt * kt[i];
+                const double wk = bt * kt[i];
                 double *row = S + i * Dv;
                 for (int64_t j = 0; j < Dv; ++j)
-                    row[j] += bk * W[j];
+                    row[j] += wk * W[j];
             }
         }
         for (int64_t j = 0; j < Dv; ++j) {

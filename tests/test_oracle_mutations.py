@@ -33,9 +33,11 @@ MUTATIONS = {
     # delta rule
     "delta_correction_dropped": ("W[j] = vt[j] - u;", "W[j] = vt[j];"),
     "delta_correction_sign": ("W[j] = vt[j] - u;", "W[j] = vt[j] + u;"),
-    "delta_no_decay": ("                    row[j] *= decay;", "                    row[j] *= 1.0;"),
+    "delta_no_decay": ("                    row[j] *= ei;", "                    row[j] *= 1.0;"),
+    "delta_decay_sign": ("const double ei = exp(gt[i]);", "const double ei = exp(-gt[i]);"),
     "delta_beta_in_correction": ("u += S[i * Dv + j] * kt[i];", "u += S[i * Dv + j] * bt * kt[i];"),
     "delta_state_transposed": ("u += S[i * Dv + j] * kt[i];", "u += S[j * Dv + i] * kt[i];"),
+    "delta_beta_dropped": ("const double wk = bt * kt[i];", "const double wk = kt[i];"),
     # gradients
     "bwd_no_adjoint_decay": ("                A[i * Dv + j] *= exp(gt[i]);",
                              "                A[i * Dv + j] *= 1.0;"),

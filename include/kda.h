@@ -264,6 +264,29 @@ kda_status_t kda_chunk_fwd_varlen_conv(const void *x_q, const void *x_k, const v
                                        uint32_t *status_dev, kda_stream_t stream);
 
 /*
+ * kda_delta_fwd_varlen -- the delta-rule form of the recurrence. [RFC-0026]
+ * names the method Kimi Delta Attention but its pages state only the additive
+ * update of kda_chunk_fwd_varlen; this is the reading of that name, the gated
+ * delta rule with a decay per key channel:
+ *     S'_t = S_{t-1} * exp(g_t)                      (key rows)
+ *     S_t  = S'_t + beta_t * k_t (v_t - S'_t^T k_t)^T  = (I - beta_t k_t k_t^T) S'_t
+ *                                                      + beta_t k_t v_t^T
+ *     o_t  = scale * S_t^T q_t
+ * with S = 0 at every segment start and padding outputs 0, as in
+ * kda_chunk_fwd_varlen. It runs the token recurrence in fp32 arithmetic (one
+ * walk per segment and head; each token's S'^T k is a reduction over the
+ * walk's threads), for either dtype; there is no chunked (tensor-core) form of
+ * it here. The arguments, layouts, workspace sizes and return codes are
+ * kda_chunk_fwd_varlen's; d_qk == d_v in {64, 128}.
+ */
+kda_status_t kda_delta_fwd_varlen(const void *q, const void *k, const void *v, const void *g,
+                                  const void *beta, const int32_t *segment_ids, int64_t B,
+                                  int64_t T, int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                  kda_dtype_t dtype, kda_dtype_t out_dtype, void *o,
+                                  void *workspace, size_t workspace_bytes, uint32_t *status_dev,
+                                  kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_varlen_state -- kda_chunk_fwd_varlen with per-segment recurrent
  * state in and out: the initial_state and output_final_state kwargs that
  * [RFC-0026] passes to the chunked KDA call, one state per packed sequence.

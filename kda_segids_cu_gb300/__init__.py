@@ -92,6 +92,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                               ctypes.c_int, vp, vp, ctypes.c_size_t, ctypes.c_int,
                                               u32p, vp]
     lib.kda_chunk_fwd_varlen_conv.restype = ctypes.c_int
+    lib.kda_delta_fwd_varlen.argtypes = lib.kda_chunk_fwd_varlen.argtypes
+    lib.kda_delta_fwd_varlen.restype = ctypes.c_int
     lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_uint64, u32p, vp]
     lib.kda_selftest_wait_timeout.restype = ctypes.c_int
     lib.kda_chunk_fwd_varlen_state.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32,
@@ -346,6 +348,30 @@ def kda_chunk_fwd_varlen_conv(x_q: torch.Tensor, x_k: torch.Tensor, x_v: torch.T
         _ptr(q), _ptr(k), _ptr(v), _ptr(ws_[0]), _ptr(ws_[1]), _ptr(ws_[2]), ws_[0].shape[0],
         _ptr(g), _ptr(beta), _ptr(seg), B, T, H, Dk, Dv, float(scale), dt, odt, _ptr(o),
         _ptr(workspace), workspace.numel(), int(planned), _ptr(status), _stream_ptr(st)))
+    if check:
+        _raise_on_status(name, status, st)
+    return o
+
+
+def kda_delta_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                         beta: torch.Tensor, segment_ids: torch.Tensor | None = None,
+                         scale: float = 1.0, B: int | None = None, T: int | None = None,
+                         stream=None, out: torch.Tensor | None = None,
+                         workspace: torch.Tensor | None = None,
+                         status: torch.Tensor | None = None,
+                         out_dtype: torch.dtype | None = None,
+                         check: bool | None = None) -> torch.Tensor:
+    """The delta-rule form of the recurrence, S_t = S'_t + beta_t k_t (v_t - S'_t^T k_t)^T
+    (the reading of the method's name; the pages state only the additive update), as a
+    token recurrence in fp32 arithmetic. Arguments as kda_chunk_fwd_varlen."""
+    q, k, v, g, beta, seg, B, T, H, Dk, Dv, dt, odt, o, workspace = _chunk_args(
+        q, k, v, g, beta, segment_ids, B, T, out, workspace, out_dtype)
+    status, check, st = _status_word(status, check, q.device, stream)
+    name = "kda_delta_fwd_varlen"
+    _check(name, load_library().kda_delta_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(seg), B, T, H, Dk, Dv,
+        float(scale), dt, odt, _ptr(o), _ptr(workspace), workspace.numel(), _ptr(status),
+        _stream_ptr(st)))
     if check:
         _raise_on_status(name, status, st)
     return o

@@ -14,6 +14,10 @@ kda_status_t launch_recurrent_state(const void* q, const void* k, const void* v,
                                     int32_t H, int32_t D, float scale, kda_dtype_t dtype,
                                     kda_dtype_t out_dtype, void* o, void* ws, const float* init,
                                     float* fin, int64_t n_state, cudaStream_t stream);
+kda_status_t launch_recurrent_delta(const void* q, const void* k, const void* v, const void* g,
+                                    const void* beta, const int32_t* seg, int64_t B, int64_t T_len,
+                                    int32_t H, int32_t D, float scale, kda_dtype_t dtype,
+                                    kda_dtype_t out_dtype, void* o, void* ws, cudaStream_t stream);
 kda_status_t launch_chunk_plan(const int32_t* seg, int64_t B, int64_t T, int32_t H, int32_t D,
                                bool with_state, void* ws, size_t ws_bytes, cudaStream_t stream);
 kda_status_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* g,
@@ -227,6 +231,21 @@ kda_status_t kda_chunk_fwd_varlen_conv(const void* x_q, const void* x_k, const v
                                 out_dtype, o, workspace, workspace_bytes, status_dev, nullptr,
                                 nullptr, 0, planned == 0, reinterpret_cast<cudaStream_t>(stream),
                                 &conv);
+}
+
+kda_status_t kda_delta_fwd_varlen(const void* q, const void* k, const void* v, const void* g,
+                                  const void* beta, const int32_t* segment_ids, int64_t B,
+                                  int64_t T, int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                  kda_dtype_t dtype, kda_dtype_t out_dtype, void* o,
+                                  void* workspace, size_t workspace_bytes, uint32_t* status_dev,
+                                  kda_stream_t stream) {
+    const kda_status_t chk = check_fwd_args(q, k, v, g, beta, segment_ids, B, T, H, d_qk, d_v,
+                                            dtype, out_dtype, o, workspace, workspace_bytes,
+                                            status_dev);
+    if (chk != KDA_OK) return chk;
+    return kda::launch_recurrent_delta(q, k, v, g, beta, segment_ids, B, T, H, d_qk, scale, dtype,
+                                       out_dtype, o, workspace,
+                                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 kda_status_t kda_chunk_fwd_varlen_state(const void* q, const void* k, const void* v,

@@ -140,12 +140,18 @@ constexpr int kTile = 8;                  // each thread holds an 8 x 8 block of
 constexpr int kWin = 8;                   // tokens staged per window
 
 template <int D> constexpr int rec_threads() { return (D / kTile) * (D / kTile); }
-template <int D> constexpr int rec_smem_bytes() {
-    // staged q, beta*k, exp(g), v per token, and per-warp partial read-outs
-    return 4 * kWin * D * 4 + (rec_threads<D>() / 32) * kWin * D * 4;
+template <int D, bool kDelta = false> constexpr int rec_smem_bytes() {
+    // staged q, beta*k, exp(g), v per token, and per-warp partial read-outs; the delta rule
+    // also stages k and exchanges per-warp partial sums of S'^T k (two buffers)
+    return 4 * kWin * D * 4 + (rec_threads<D>() / 32) * kWin * D * 4 +
+           (kDelta ? kWin * D * 4 + 2 * (rec_threads<D>() / 32) * D * 4 : 0);
 }
 
-template <typename T, typename To, int D>
+// kDelta: the delta rule, the reading of the method's name (the pages state only the
+// additive update above): S'_t = S_{t-1} exp(g_t), S_t = S'_t + beta_t k_t (v_t - S'_t^T k_t)^T.
+// Each token's u = S'^T k sums over all key rows, so the CTA meets once per token: the
+// warps' partial sums go through shared memory (two buffers, by token parity).
+template <typename T, typename To, int D, bool kDelta>
 __global__ void __launch_bounds__(rec_threads<D>(), D == 64 ? 8 : 2)
 recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                  const T* __restrict__ g, const T* __restrict__ beta, int32_t H, float scale,
@@ -161,6 +167,8 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
     float* se = sbk + kWin * D;
     float* sv = se + kWin * D;
     float* part = sv + kWin * D;          // [NW][kWin][D]
+    float* sk = part + NW * kWin * D;     // delta rule: [kWin][D] k
+    float* upart = sk + kWin * D;         // delta rule: [2][NW][D] partial S'^T k
 
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
@@ -219,6 +227,7 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                     sbk[e] = rb[m] * rk[m];
                     se[e] = expf(rg_[m]);
                     sv[e] = rv[m];
+                    if constexpr (kDelta) sk[e] = rk[m];
                 }
             }
             load_window(pw + kWin);   // in flight while this window is computed
@@ -240,15 +249,72 @@ recurrent_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
                 float2 acc[kTile / 2];
 #pragma unroll
                 for (int jp = 0; jp < kTile / 2; ++jp) acc[jp] = make_float2(0.f, 0.f);
+                if constexpr (!kDelta) {
 #pragma unroll
-                for (int i = 0; i < kTile; ++i) {
-                    const float2 e2 = make_float2(ei[i], ei[i]);
-                    const float2 b2 = make_float2(bi[i], bi[i]);
-                    const float2 q2 = make_float2(qi[i], qi[i]);
+                    for (int i = 0; i < kTile; ++i) {
+                        const float2 e2 = make_float2(ei[i], ei[i]);
+                        const float2 b2 = make_float2(bi[i], bi[i]);
+                        const float2 q2 = make_float2(qi[i], qi[i]);
 #pragma unroll
-                    for (int jp = 0; jp < kTile / 2; ++jp) {
-                        S[i][jp] = rfma2(S[i][jp], e2, rmul2(b2, vj[jp]));   // decay, then add
-                        acc[jp] = rfma2(q2, S[i][jp], acc[jp]);              // read-out after
+                        for (int jp = 0; jp < kTile / 2; ++jp) {
+                            S[i][jp] = rfma2(S[i][jp], e2, rmul2(b2, vj[jp]));   // decay, then add
+                            acc[jp] = rfma2(q2, S[i][jp], acc[jp]);              // read-out after
+                        }
+                    }
+                } else {
+                    // decay, and this thread's part of u = S'^T k (its 8 key rows)
+                    const float4* kr4 = reinterpret_cast<const float4*>(sk + w * D + kTile * rg);
+                    const float4 k0 = kr4[0], k1 = kr4[1];
+                    const float ki[kTile] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+                    float2 pu[kTile / 2];
+#pragma unroll
+                    for (int jp = 0; jp < kTile / 2; ++jp) pu[jp] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < kTile; ++i) {
+                        const float2 e2 = make_float2(ei[i], ei[i]);
+                        const float2 k2 = make_float2(ki[i], ki[i]);
+#pragma unroll
+                        for (int jp = 0; jp < kTile / 2; ++jp) {
+                            S[i][jp] = rmul2(S[i][jp], e2);
+                            pu[jp] = rfma2(k2, S[i][jp], pu[jp]);
+                        }
+                    }
+                    // sum over the warp's row groups, then over the warps through shared memory
+#pragma unroll
+                    for (int m = NG; m < 32; m <<= 1) {
+#pragma unroll
+                        for (int jp = 0; jp < kTile / 2; ++jp) {
+                            pu[jp].x += __shfl_xor_sync(0xffffffffu, pu[jp].x, m);
+                            pu[jp].y += __shfl_xor_sync(0xffffffffu, pu[jp].y, m);
+                        }
+                    }
+                    float* ub = upart + (w & 1) * NW * D;
+                    if (lane < NG) {
+                        float4* dst = reinterpret_cast<float4*>(ub + warp * D + kTile * cg);
+                        dst[0] = make_float4(pu[0].x, pu[0].y, pu[1].x, pu[1].y);
+                        dst[1] = make_float4(pu[2].x, pu[2].y, pu[3].x, pu[3].y);
+                    }
+                    __syncthreads();
+                    float2 dv[kTile / 2];
+#pragma unroll
+                    for (int jp = 0; jp < kTile / 2; ++jp) dv[jp] = vj[jp];
+#pragma unroll
+                    for (int wp = 0; wp < NW; ++wp) {
+                        const float4* src = reinterpret_cast<const float4*>(ub + wp * D + kTile * cg);
+                        const float4 a = src[0], b = src[1];
+                        dv[0].x -= a.x; dv[0].y -= a.y; dv[1].x -= a.z; dv[1].y -= a.w;
+                        dv[2].x -= b.x; dv[2].y -= b.y; dv[3].x -= b.z; dv[3].y -= b.w;
+                    }
+                    // S = S' + beta k (v - u)^T, then the read-out
+#pragma unroll
+                    for (int i = 0; i < kTile; ++i) {
+                        const float2 b2 = make_float2(bi[i], bi[i]);
+                        const float2 q2 = make_float2(qi[i], qi[i]);
+#pragma unroll
+                        for (int jp = 0; jp < kTile / 2; ++jp) {
+                            S[i][jp] = rfma2(b2, dv[jp], S[i][jp]);
+                            acc[jp] = rfma2(q2, S[i][jp], acc[jp]);
+                        }
                     }
                 }
                 // sum the partial read-outs of the warp's row groups, then one store per column
@@ -306,7 +372,7 @@ kda_status_t launch_segment_list(const int32_t* seg, int64_t B, int64_t T_len, v
     return launch_status();
 }
 
-template <typename T, typename To>
+template <typename T, typename To, bool kDelta>
 static kda_status_t launch_recurrent_typed(const void* q, const void* k, const void* v,
                                            const void* g, const void* beta, const int32_t* seg,
                                            int64_t B, int64_t T_len, int32_t H, int32_t D,
@@ -330,18 +396,37 @@ static kda_status_t launch_recurrent_typed(const void* q, const void* k, const v
     const T* bp = static_cast<const T*>(beta);
     To* op = static_cast<To*>(o);
     if (D == 64) {
-        if (dynamic_smem_attr<recurrent_kernel<T, To, 64>>(rec_smem_bytes<64>()) != cudaSuccess)
+        constexpr int smem = rec_smem_bytes<64, kDelta>();
+        if (dynamic_smem_attr<recurrent_kernel<T, To, 64, kDelta>>(smem) != cudaSuccess)
             return KDA_ERR_CUDA;
-        recurrent_kernel<T, To, 64><<<blocks, rec_threads<64>(), rec_smem_bytes<64>(), stream>>>(
+        recurrent_kernel<T, To, 64, kDelta><<<blocks, rec_threads<64>(), smem, stream>>>(
             qp, kp, vp, gp, bp, H, scale, seg_start, seg_end, counters, op, init, fin, n_state);
     } else {
-        if (dynamic_smem_attr<recurrent_kernel<T, To, 128>>(rec_smem_bytes<128>()) != cudaSuccess)
+        constexpr int smem = rec_smem_bytes<128, kDelta>();
+        if (dynamic_smem_attr<recurrent_kernel<T, To, 128, kDelta>>(smem) != cudaSuccess)
             return KDA_ERR_CUDA;
-        recurrent_kernel<T, To, 128><<<blocks, rec_threads<128>(), rec_smem_bytes<128>(),
-                                       stream>>>(qp, kp, vp, gp, bp, H, scale, seg_start, seg_end,
-                                                 counters, op, init, fin, n_state);
+        recurrent_kernel<T, To, 128, kDelta><<<blocks, rec_threads<128>(), smem, stream>>>(
+            qp, kp, vp, gp, bp, H, scale, seg_start, seg_end, counters, op, init, fin, n_state);
     }
     return launch_status();
+}
+
+template <bool kDelta>
+static kda_status_t launch_recurrent_dtypes(const void* q, const void* k, const void* v,
+                                            const void* g, const void* beta, const int32_t* seg,
+                                            int64_t B, int64_t T_len, int32_t H, int32_t D,
+                                            float scale, kda_dtype_t dtype, kda_dtype_t out_dtype,
+                                            void* o, void* ws, const float* init, float* fin,
+                                            int64_t n_state, cudaStream_t stream) {
+    if (dtype == KDA_BF16) {
+        if (out_dtype == KDA_F32)
+            return launch_recurrent_typed<__nv_bfloat16, float, kDelta>(
+                q, k, v, g, beta, seg, B, T_len, H, D, scale, o, ws, init, fin, n_state, stream);
+        return launch_recurrent_typed<__nv_bfloat16, __nv_bfloat16, kDelta>(
+            q, k, v, g, beta, seg, B, T_len, H, D, scale, o, ws, init, fin, n_state, stream);
+    }
+    return launch_recurrent_typed<float, float, kDelta>(q, k, v, g, beta, seg, B, T_len, H, D,
+                                                        scale, o, ws, init, fin, n_state, stream);
 }
 
 kda_status_t launch_recurrent_state(const void* q, const void* k, const void* v, const void* g,
@@ -349,17 +434,17 @@ kda_status_t launch_recurrent_state(const void* q, const void* k, const void* v,
                                     int32_t H, int32_t D, float scale, kda_dtype_t dtype,
                                     kda_dtype_t out_dtype, void* o, void* ws, const float* init,
                                     float* fin, int64_t n_state, cudaStream_t stream) {
-    if (dtype == KDA_BF16) {
-        if (out_dtype == KDA_F32)
-            return launch_recurrent_typed<__nv_bfloat16, float>(q, k, v, g, beta, seg, B, T_len,
-                                                                H, D, scale, o, ws, init, fin,
-                                                                n_state, stream);
-        return launch_recurrent_typed<__nv_bfloat16, __nv_bfloat16>(q, k, v, g, beta, seg, B,
-                                                                    T_len, H, D, scale, o, ws,
-                                                                    init, fin, n_state, stream);
-    }
-    return launch_recurrent_typed<float, float>(q, k, v, g, beta, seg, B, T_len, H, D, scale, o,
-                                                ws, init, fin, n_state, stream);
+    return launch_recurrent_dtypes<false>(q, k, v, g, beta, seg, B, T_len, H, D, scale, dtype,
+                                          out_dtype, o, ws, init, fin, n_state, stream);
+}
+
+// The delta-rule recurrence (the reading of the method's name), every segment from zero.
+kda_status_t launch_recurrent_delta(const void* q, const void* k, const void* v, const void* g,
+                                    const void* beta, const int32_t* seg, int64_t B, int64_t T_len,
+                                    int32_t H, int32_t D, float scale, kda_dtype_t dtype,
+                                    kda_dtype_t out_dtype, void* o, void* ws, cudaStream_t stream) {
+    return launch_recurrent_dtypes<true>(q, k, v, g, beta, seg, B, T_len, H, D, scale, dtype,
+                                         out_dtype, o, ws, nullptr, nullptr, 0, stream);
 }
 
 kda_status_t launch_recurrent(const void* q, const void* k, const void* v, const void* g,

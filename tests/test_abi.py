@@ -71,7 +71,8 @@ def test_conv_rejects_invalid_arguments(lib):
     assert f(FAKE, FAKE, None, FAKE, 1, 4, 8, 4, 3, None) == -1     # dtype
 
 
-@pytest.mark.parametrize("fname", ["kda_chunk_fwd_varlen", "kda_chunk_fwd_varlen_planned"])
+@pytest.mark.parametrize("fname", ["kda_chunk_fwd_varlen", "kda_chunk_fwd_varlen_planned",
+                                   "kda_delta_fwd_varlen"])
 def test_chunk_rejects_invalid_arguments(lib, fname):
     f = getattr(lib, fname)
     ws = lib.kda_chunk_fwd_varlen_workspace_min(1, 64, 2, 64, 64, kda.KDA_BF16)

@@ -328,9 +328,12 @@ kda_status_t kda_chunk_fwd_varlen_state(const void *q, const void *k, const void
 
 /*
  * kda_chunk_bwd_varlen_workspace_size -- bytes of device scratch that
- * kda_chunk_bwd_varlen needs (0 on invalid or unsupported sizes): the segment
- * list, dq in fp32 and one fp32 state per 64-token chunk and head, about
- * (B*T) * H * (4 d_qk + 4 d_qk d_v / 64) bytes.
+ * kda_chunk_bwd_varlen and kda_chunk_bwd_varlen_ex need, with either method (0 on
+ * invalid or unsupported sizes). The fp32 walks keep the segment list, dq in
+ * fp32 and one fp32 state per 64-token chunk and head, about
+ * (B*T) * H * (4 d_qk + 4 d_qk d_v / 64) bytes; the tensor-core path keeps two
+ * fp32 states per chunk and head (the state entering the chunk and the adjoint
+ * at its end), about (B*T) * H * 8 d_qk d_v / 64 bytes. The size is the larger.
  */
 size_t kda_chunk_bwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int32_t d_qk,
                                            int32_t d_v, kda_dtype_t dtype);
@@ -356,8 +359,7 @@ size_t kda_chunk_bwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int3
  *   dv           device [B*T, H, d_v] of `grad_dtype`
  *   dbeta        device [B*T, H] of `grad_dtype`
  *   grad_dtype   KDA_F32, or equal to `dtype`; values rounded once to nearest even
- * It runs in fp32 arithmetic as two walks per (segment, head): forward for dq
- * and the chunk-start states, then backward for the rest, which reads them back.
+ * It is kda_chunk_bwd_varlen_ex with method KDA_BWD_AUTO and no status word.
  *
  * Returns KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE or
  * KDA_ERR_CUDA. Calls that share a workspace must not overlap in time.
@@ -368,6 +370,42 @@ kda_status_t kda_chunk_bwd_varlen(const void *q, const void *k, const void *v, c
                                   kda_dtype_t dtype, const void *d_o, kda_dtype_t grad_dtype,
                                   void *dq, void *dk, void *dv, void *dg, void *dbeta,
                                   void *workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/* Methods of kda_chunk_bwd_varlen_ex. */
+#define KDA_BWD_AUTO 0 /* tensor cores for bf16 inputs with d_qk = d_v = 128, else the walks */
+#define KDA_BWD_WALK 1 /* the fp32 walks, for every supported shape and dtype */
+
+/*
+ * kda_chunk_bwd_varlen_ex -- kda_chunk_bwd_varlen with a choice of method and a
+ * device status word. Arguments and results are kda_chunk_bwd_varlen's, plus:
+ *   method       KDA_BWD_AUTO or KDA_BWD_WALK (anything else: KDA_ERR_INVALID_ARG)
+ *   status_dev   device uint32, nullable: KDA_DEV_* bits are ORed into it, as in
+ *                kda_chunk_fwd_varlen
+ *
+ * KDA_BWD_WALK runs in fp32 arithmetic as two walks per (segment, head): forward
+ * for dq and the chunk-start states, then backward for the rest, which reads
+ * them back. Its gradients hold the fp32 bound (1e-4 RMS per head).
+ *
+ * KDA_BWD_AUTO, for bf16 inputs with d_qk = d_v = 128, runs the chunked form on
+ * tcgen05 tensor cores in three launches: a forward scan over the chunks that
+ * one segment links stores the state entering every chunk; a backward scan
+ * stores the adjoint at every chunk's end; then, per (chunk, head) and with no
+ * dependence between them, eight tensor-core products give dq, dk, dv, and the
+ * epilogue dg and dbeta (dg from its sum within the chunk plus the direct form
+ * past it). Operands are bf16 (decayed ones as hi + lo pairs), accumulation
+ * fp32, as in the forward kernel, so the gradients hold the bf16 bound of the
+ * forward's output (2e-2 RMS per head). As in the forward's whole-chunk form,
+ * a chunk whose log-decay on some key channel falls below -80 sets
+ * KDA_DEV_DECAY_RANGE and its gradients are unreliable: use KDA_BWD_WALK there.
+ * Other inputs take the walks.
+ */
+kda_status_t kda_chunk_bwd_varlen_ex(const void *q, const void *k, const void *v, const void *g,
+                                     const void *beta, const int32_t *segment_ids, int64_t B,
+                                     int64_t T, int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                     kda_dtype_t dtype, const void *d_o, kda_dtype_t grad_dtype,
+                                     void *dq, void *dk, void *dv, void *dg, void *dbeta,
+                                     void *workspace, size_t workspace_bytes, int32_t method,
+                                     uint32_t *status_dev, kda_stream_t stream);
 
 /*
  * kda_chunk_fwd_varlen_noalloc -- kda_chunk_fwd_varlen for callers that cannot

@@ -104,6 +104,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                          ctypes.c_float, ctypes.c_int, vp, ctypes.c_int, vp, vp,
                                          vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.kda_chunk_bwd_varlen.restype = ctypes.c_int
+    lib.kda_chunk_bwd_varlen_ex.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32,
+                                            ctypes.c_float, ctypes.c_int, vp, ctypes.c_int, vp,
+                                            vp, vp, vp, vp, vp, ctypes.c_size_t, i32, u32p, vp]
+    lib.kda_chunk_bwd_varlen_ex.restype = ctypes.c_int
     lib.kda_chunk_bwd_varlen_workspace_size.argtypes = [i64, i64, i32, i32, i32, ctypes.c_int]
     lib.kda_chunk_bwd_varlen_workspace_size.restype = ctypes.c_size_t
     if path is None:
@@ -449,15 +453,27 @@ def kda_chunk_fwd_varlen_state(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
     return o, fin
 
 
+KDA_BWD_AUTO = 0
+KDA_BWD_WALK = 1
+_BWD_METHODS = {"auto": KDA_BWD_AUTO, "walk": KDA_BWD_WALK}
+
+
 def kda_chunk_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
                          beta: torch.Tensor, d_o: torch.Tensor,
                          segment_ids: torch.Tensor | None = None, scale: float = 1.0,
                          B: int | None = None, T: int | None = None, stream=None,
                          workspace: torch.Tensor | None = None,
-                         grad_dtype: torch.dtype | None = None):
+                         grad_dtype: torch.dtype | None = None, method: str = "auto",
+                         status: torch.Tensor | None = None, check: bool | None = None):
     """Gradients of kda_chunk_fwd_varlen for the upstream gradient d_o (shaped like v, of
     the input dtype). Returns (dq, dk, dv, dg, dbeta) shaped like q, k, v, g, beta, of
-    `grad_dtype` (default: the input dtype; float32 is also accepted)."""
+    `grad_dtype` (default: the input dtype; float32 is also accepted).
+
+    method="auto" runs bf16 inputs with 128-wide heads on the tensor-core path (the bf16
+    bound) and everything else on the fp32 walks; method="walk" forces the walks (the fp32
+    bound). The device status word is handled as in kda_chunk_fwd_varlen."""
+    if method not in _BWD_METHODS:
+        raise ValueError(f"method must be one of {sorted(_BWD_METHODS)}")
     q, k, v, g, beta, seg, B, T, H, Dk, Dv, dt, _, _, workspace = _chunk_args(
         q, k, v, g, beta, segment_ids, B, T, None, workspace, None,
         workspace_size=load_library().kda_chunk_bwd_varlen_workspace_size, want_out=False)
@@ -468,12 +484,16 @@ def kda_chunk_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: t
     gdt = _dtype_code(grad_dtype)
     dq, dk, dv, dg, db = (torch.empty(t.shape, dtype=grad_dtype, device=q.device)
                           for t in (q, k, v, g, beta))
+    status, check, st = _status_word(status, check, q.device, stream)
     _check("kda_chunk_bwd_varlen",
-           load_library().kda_chunk_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                                               _ptr(seg), B, T, H, Dk, Dv, float(scale), dt,
-                                               _ptr(d_o), gdt, _ptr(dq), _ptr(dk), _ptr(dv),
-                                               _ptr(dg), _ptr(db), _ptr(workspace),
-                                               workspace.numel(), _stream_ptr(stream)))
+           load_library().kda_chunk_bwd_varlen_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                                  _ptr(seg), B, T, H, Dk, Dv, float(scale), dt,
+                                                  _ptr(d_o), gdt, _ptr(dq), _ptr(dk), _ptr(dv),
+                                                  _ptr(dg), _ptr(db), _ptr(workspace),
+                                                  workspace.numel(), _BWD_METHODS[method],
+                                                  _ptr(status), _stream_ptr(st)))
+    if check:
+        _raise_on_status("kda_chunk_bwd_varlen", status, st)
     return dq, dk, dv, dg, db
 
 

@@ -32,6 +32,12 @@ kda_status_t launch_bwd(const void* q, const void* k, const void* v, const void*
                         int64_t T_len, int32_t H, int32_t D, float scale, kda_dtype_t dtype,
                         kda_dtype_t grad_dtype, void* dq, void* dk, void* dv, void* dg,
                         void* dbeta, void* ws, cudaStream_t stream);
+size_t bwd_tc_workspace_bytes(int64_t N, int32_t H);
+kda_status_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* g,
+                           const void* beta, const void* d_o, const int32_t* seg, int64_t B,
+                           int64_t T_len, int32_t H, float scale, kda_dtype_t grad_dtype,
+                           void* dq, void* dk, void* dv, void* dg, void* dbeta, void* ws,
+                           uint32_t* status_dev, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -289,7 +295,42 @@ size_t kda_chunk_bwd_varlen_workspace_size(int64_t B, int64_t T, int32_t H, int3
                                            int32_t d_v, kda_dtype_t dtype) {
     if (!token_count_ok(B, T) || H < 1 || d_qk < 1 || d_v < 1 || !valid_dtype(dtype)) return 0;
     if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return 0;
-    return kda::bwd_workspace_bytes(B * T, H, d_qk);
+    const size_t walk = kda::bwd_workspace_bytes(B * T, H, d_qk);
+    if (dtype != KDA_BF16 || d_qk != 128) return walk;
+    const size_t tc = kda::bwd_tc_workspace_bytes(B * T, H);
+    return walk > tc ? walk : tc;
+}
+
+kda_status_t kda_chunk_bwd_varlen_ex(const void* q, const void* k, const void* v, const void* g,
+                                     const void* beta, const int32_t* segment_ids, int64_t B,
+                                     int64_t T, int32_t H, int32_t d_qk, int32_t d_v, float scale,
+                                     kda_dtype_t dtype, const void* d_o, kda_dtype_t grad_dtype,
+                                     void* dq, void* dk, void* dv, void* dg, void* dbeta,
+                                     void* workspace, size_t workspace_bytes, int32_t method,
+                                     uint32_t* status_dev, kda_stream_t stream) {
+    if (!q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta)
+        return KDA_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !valid_dtype(grad_dtype) || !token_count_ok(B, T) || H < 1 ||
+        d_qk < 1 || d_v < 1)
+        return KDA_ERR_INVALID_ARG;
+    if (method != KDA_BWD_AUTO && method != KDA_BWD_WALK) return KDA_ERR_INVALID_ARG;
+    if (grad_dtype != dtype && grad_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return KDA_ERR_UNSUPPORTED;
+    if (int64_t(H) * d_qk > 65536) return KDA_ERR_UNSUPPORTED;
+    const void* ptrs[] = {q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta};
+    for (const void* p : ptrs)
+        if (!kda::aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (segment_ids && !kda::aligned(segment_ids, 4)) return KDA_ERR_INVALID_ARG;
+    if (status_dev && !kda::aligned(status_dev, 4)) return KDA_ERR_INVALID_ARG;
+    const size_t need = kda_chunk_bwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
+    if (!workspace || workspace_bytes < need || !kda::aligned(workspace, 256))
+        return KDA_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (method == KDA_BWD_AUTO && dtype == KDA_BF16 && d_qk == 128)
+        return kda::launch_bwd_tc(q, k, v, g, beta, d_o, segment_ids, B, T, H, scale, grad_dtype,
+                                  dq, dk, dv, dg, dbeta, workspace, status_dev, st);
+    return kda::launch_bwd(q, k, v, g, beta, d_o, segment_ids, B, T, H, d_qk, scale, dtype,
+                           grad_dtype, dq, dk, dv, dg, dbeta, workspace, st);
 }
 
 kda_status_t kda_chunk_bwd_varlen(const void* q, const void* k, const void* v, const void* g,
@@ -298,24 +339,9 @@ kda_status_t kda_chunk_bwd_varlen(const void* q, const void* k, const void* v, c
                                   kda_dtype_t dtype, const void* d_o, kda_dtype_t grad_dtype,
                                   void* dq, void* dk, void* dv, void* dg, void* dbeta,
                                   void* workspace, size_t workspace_bytes, kda_stream_t stream) {
-    if (!q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta)
-        return KDA_ERR_INVALID_ARG;
-    if (!valid_dtype(dtype) || !valid_dtype(grad_dtype) || !token_count_ok(B, T) || H < 1 ||
-        d_qk < 1 || d_v < 1)
-        return KDA_ERR_INVALID_ARG;
-    if (grad_dtype != dtype && grad_dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
-    if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return KDA_ERR_UNSUPPORTED;
-    if (int64_t(H) * d_qk > 65536) return KDA_ERR_UNSUPPORTED;
-    const void* ptrs[] = {q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta};
-    for (const void* p : ptrs)
-        if (!kda::aligned(p, 16)) return KDA_ERR_INVALID_ARG;
-    if (segment_ids && !kda::aligned(segment_ids, 4)) return KDA_ERR_INVALID_ARG;
-    const size_t need = kda_chunk_bwd_varlen_workspace_size(B, T, H, d_qk, d_v, dtype);
-    if (!workspace || workspace_bytes < need || !kda::aligned(workspace, 256))
-        return KDA_ERR_WORKSPACE;
-    return kda::launch_bwd(q, k, v, g, beta, d_o, segment_ids, B, T, H, d_qk, scale, dtype,
-                           grad_dtype, dq, dk, dv, dg, dbeta, workspace,
-                           reinterpret_cast<cudaStream_t>(stream));
+    return kda_chunk_bwd_varlen_ex(q, k, v, g, beta, segment_ids, B, T, H, d_qk, d_v, scale,
+                                   dtype, d_o, grad_dtype, dq, dk, dv, dg, dbeta, workspace,
+                                   workspace_bytes, KDA_BWD_AUTO, nullptr, stream);
 }
 
 }  // extern "C"

@@ -1,0 +1,1221 @@
+// kda_bwd_tc.cu -- bf16 path of kda_chunk_bwd_varlen (d_qk = d_v = 128): the gradients of the
+// chunked KDA forward on tcgen05 tensor cores.
+//
+// Method: [RFC-0026] "RFC-0026: Ling3 KDA Varlen 支持（packing 文档间隔离）", 背景 "KDA 状态泄漏问题"
+// (S_t = S_{t-1} exp(g_t) + beta_t k_t v_t^T with rows = key channels, o_t = scale S_t^T q_t) and
+// §3.1.1 (S = 0 at every segment start, id 0 = padding). The pages state the forward only; the
+// backward is its derivative (the same equations as the fp32 walks of kda_bwd.cu), organised by
+// 64-token chunks:
+//
+//   per chunk c and head: S_in = the state its carried segment brings in (row = key channel),
+//   D_end = dL/dS at the chunk's last token for the segment that goes on into chunk c + 1.
+//   Within the chunk (tokens t, s; Suf_t = sum of g over the chunk's real tokens after t;
+//   Qt_t = q_t exp(-Suf_t), Ktb_s = beta_s k_s exp(Suf_s), as in the forward kernel):
+//     M_ts  = 1 when t is real and s lies in t's segment with s <= t
+//     A'    = scale * M . (Qt Ktb^T)          W = M . (dO V^T)
+//     dq_t  = scale exp(-Suf_t) [ (W Ktb)_t + [t carried] S_dec do_t ],   S_dec = diag(P) S_in
+//     dk_s  = beta_s exp(Suf_s) [ scale (W^T Qt)_s + [s in the last segment] D_end v_s ]
+//     dv_s  = (A'^T dO)_s + [s in the last segment] D_end^T Ktb_s
+//     dbeta_s = k_s . (dk_s / beta_s)
+//     dg_t  = sum over u >= t of t's segment within the chunk of (q_u dq_u - k_u dk_u)
+//             + [t in the last segment] sum_j S_out[i][j] D_end[i][j]      (per channel i)
+//   where P = exp(sum of the chunk's real g), S_out = the state at the chunk's end; dg is 0 at a
+//   segment's first token (g_t there multiplies a zero state).
+//   The last line is the identity dL/dG_u = q_u dq_u - k_u dk_u (o depends on the cumulative
+//   log-decay G only through G_t - G_s), summed over the tokens whose G g_t enters; the part
+//   past the chunk is the direct form of dg at the next chunk's first token.
+//
+// Three launches after a small planner:
+//   scan_kernel<false>  walks each chain of chunks that one segment links (a chunk holding a
+//     start or padding begins a chain) forward in time and stores S_in of every chunk:
+//     S^T (+)= V^T Khat with Khat = beta k exp(Suf) on the rows that reach the chunk's end.
+//   scan_kernel<true>   walks the same chains backward and stores D_end:
+//     D^T = D^T diag(P) + dO^T Qhat, Qhat_t = scale q_t exp(G_t) on the rows of the segment the
+//     chunk carries in (G_t = sum of g over the chunk's first t + 1 tokens).
+//   grad_kernel         one (chunk, head) at a time, all gradients (eight MMAs, below).
+// The scans keep the state in tensor memory (fp32) and export it per chunk; the exponentials
+// there stay within (0, 1], so they need no range check. The gradient kernel's factors
+// exp(-Suf) and exp(Suf) do: a chunk whose log-decay on some channel falls below -80 sets
+// KDA_DEV_DECAY_RANGE (its gradients are then unreliable).
+//
+// Precision: as in the forward kernel, Qt, Ktb, A' and W are carried as hi + lo bf16 pairs and
+// each product sums the pairs' cross terms; dO and V enter exactly. S_dec and D_end are hi + lo
+// pairs too: rounded once to bf16 (as the forward rounds its S_dec), S_dec alone puts dq's worst
+// error at 1.24x the bound on a chunk between two carried ones (fp64 emulation), D_end dk's at
+// 0.6x. Accumulation is fp32 in tensor memory.
+//
+// Gradient-kernel tensor-core mapping (kind::f16, transposed outputs: lane = channel, column =
+// token, so that the epilogue's suffix sum over tokens runs within a thread):
+//   SC    = Qt Ktb^T          M=64  N=64 K=128  A, B K-major                     x3
+//   W     = dO V^T            M=64  N=64 K=128  A, B K-major                     x1
+//   Qs^T  = S_dec dO^T        M=128 N=64 K=128  A K-major (128 rows), B K-major  x2
+//   T2^T  = D_end V^T         M=128 N=64 K=128  A K-major (128 rows), B K-major  x2
+//   Vs^T  = D_end^T Ktb^T     M=128 N=64 K=128  A MN-major, B K-major            x3
+//   dQ^T  = Ktb^T W^T         M=128 N=64 K=64   A MN-major, B K-major            x3
+//   dK^T  = Qt^T W            M=128 N=64 K=64   A MN-major, B MN-major           x3
+//   dV^T  = dO^T A'           M=128 N=64 K=64   A MN-major, B MN-major           x2
+// Warp roles (320 threads): 0 TMA producer, 1 MMA issuer, 2-5 prologue (one key channel per
+// thread: Suf, Qt and Ktb), 6-9 the states' conversion, the A' and W tiles and the epilogue.
+// Shared memory holds one item (224 KB of tiles); the lo halves of S_dec and D_end borrow the
+// k and g tiles (free once the prologue has read them; the epilogue reads k and g from L2) and
+// the A' and W tiles (written only after the products that read D_end_lo have completed).
+#include "kda_common.cuh"
+#include "kda_plan.cuh"
+#include "kda_sm100.cuh"
+
+namespace kda {
+namespace tc {
+bool make_map(CUtensorMap* map, const void* base, int64_t N, int32_t H);   // kda_chunk_tc.cu
+}
+
+namespace tcb {
+
+using namespace kda::sm100;
+using tc::ChunkMeta;
+using tc::align256;
+
+constexpr int D = 128;
+constexpr int C = kChunk;
+constexpr uint32_t kTile = C * D * 2;        // 16 KB: 64 rows x 128 bf16, two 8 KB panels
+constexpr uint32_t kPanel = kTile / 2;
+constexpr uint32_t kTile128 = D * D * 2;     // 32 KB: 128 rows x 128 bf16, two 16 KB panels
+constexpr uint32_t kPanel128 = kTile128 / 2;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRangeLog2 = -80.f * kLog2e;  // a chunk's log-decay below -80, in base 2
+constexpr size_t kStateBytes = size_t(D) * D * 4;
+
+// ---- workspace ------------------------------------------------------------------------
+
+struct BPlan {
+    int32_t* counters;     // [0] chains, [1] next forward-scan item, [2] next reverse-scan item
+    ChunkMeta* meta;       // [n_chunks] start / real-token masks
+    int32_t* first_cut;    // [n_chunks] first start-or-padding row, 64 if none
+    int2* chains;          // [n_chunks] (first chunk, chunk after the last)
+    int32_t* order;        // [n_chunks] chains, longest first
+    float* s_in;           // [n_chunks][H][128][128] state entering the chunk (row = key channel)
+    float* d_end;          // [n_chunks][H][128][128] adjoint at the chunk's end (row = key channel)
+};
+
+__host__ __device__ inline size_t bplan_bytes(int64_t n_chunks) {
+    return align256(64 * 4) + align256(size_t(n_chunks) * sizeof(ChunkMeta)) +
+           align256(size_t(n_chunks) * 4) * 2 + align256(size_t(n_chunks) * 8);
+}
+
+__host__ __device__ inline BPlan bplan_view(void* ws, int64_t n_chunks, int32_t H) {
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    BPlan pl;
+    pl.counters = reinterpret_cast<int32_t*>(p);   p += align256(64 * 4);
+    pl.meta = reinterpret_cast<ChunkMeta*>(p);     p += align256(size_t(n_chunks) * sizeof(ChunkMeta));
+    pl.first_cut = reinterpret_cast<int32_t*>(p);  p += align256(size_t(n_chunks) * 4);
+    pl.order = reinterpret_cast<int32_t*>(p);      p += align256(size_t(n_chunks) * 4);
+    pl.chains = reinterpret_cast<int2*>(p);        p += align256(size_t(n_chunks) * 8);
+    pl.s_in = reinterpret_cast<float*>(p);         p += size_t(n_chunks) * H * kStateBytes;
+    pl.d_end = reinterpret_cast<float*>(p);
+    return pl;
+}
+
+// ---- small device helpers -------------------------------------------------------------
+
+// Byte offset of element (r, ch) of a 64-row x 128-column K-major 128B-swizzled tile.
+__device__ __forceinline__ uint32_t eoff(int r, int ch) {
+    return (ch >> 6) * kPanel + r * 128 + ((((ch >> 3) & 7) ^ (r & 7)) << 4) + (ch & 7) * 2;
+}
+// ... of a 128-row x 128-column tile (two 16 KB panels of 128-byte rows).
+__device__ __forceinline__ uint32_t eoff128(int r, int ch) {
+    return (ch >> 6) * kPanel128 + r * 128 + ((((ch >> 3) & 7) ^ (r & 7)) << 4) + (ch & 7) * 2;
+}
+
+__device__ __forceinline__ float ld_bf(const uint8_t* base, uint32_t off) {
+    return __uint_as_float(uint32_t(*reinterpret_cast<const uint16_t*>(base + off)) << 16);
+}
+__device__ __forceinline__ void st_bf(uint8_t* base, uint32_t off, uint32_t bits16) {
+    *reinterpret_cast<uint16_t*>(base + off) = uint16_t(bits16);
+}
+__device__ __forceinline__ uint32_t bf_bits(float x) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(x);
+    return uint32_t(*reinterpret_cast<const uint16_t*>(&b));
+}
+__device__ __forceinline__ float bf_val(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+// x = hi + lo, hi = bf16(x), lo = bf16(x - hi)
+__device__ __forceinline__ void split1(float x, uint32_t& hi, uint32_t& lo) {
+    hi = bf_bits(x);
+    lo = bf_bits(x - bf_val(hi));
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = pack2(a, b);
+    lo = pack2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
+}
+// 2^x on the multi-function unit (ex2.approx: within 2 ulp)
+__device__ __forceinline__ float ex2a(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
+    if (status) atomicOr(status, bit);
+}
+
+// 32x32b shape, 16 consecutive columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// 32x32b shape, 8 consecutive columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+// Barrier 1 among the four epilogue warps only.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Rows s of t's segment with s <= t (bit s), none when t is padding.
+__device__ __forceinline__ unsigned long long keep_bits(unsigned long long start,
+                                                        unsigned long long valid, int t) {
+    if (!((valid >> t) & 1ull)) return 0ull;
+    const unsigned long long upto = (t == 63) ? ~0ull : ((2ull << t) - 1ull);
+    const unsigned long long st = start & upto;
+    const int lo = st ? 63 - __clzll((long long)st) : 0;
+    return upto & (~0ull << lo);
+}
+
+// K-major descriptor offsets (in 16-byte units) of K step kk (16 elements) of a 128-wide K:
+// 32 bytes within a 128-byte row, then the next panel.
+__device__ __forceinline__ uint64_t kofs64(int kk) {
+    return uint64_t(((kk >> 2) * kPanel + (kk & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t kofs128(int kk) {
+    return uint64_t(((kk >> 2) * kPanel128 + (kk & 3) * 32) >> 4);
+}
+
+// ---- planner ----------------------------------------------------------------------------
+
+// Per chunk: the start and real-token masks (one warp per chunk, ballots) and the first
+// start-or-padding row.
+__global__ void __launch_bounds__(256)
+bwd_masks_kernel(const int32_t* __restrict__ seg, int64_t N, RowStartTest row_start,
+                 int64_t n_chunks, void* ws) {
+    BPlan pl = bplan_view(ws, n_chunks, 0);
+    const int lane = threadIdx.x & 31;
+    const int64_t c = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (c >= n_chunks) return;
+    bool st[2], va[2];
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+        const int64_t p = c * C + hlf * 32 + lane;
+        va[hlf] = p < N && is_real(seg, p);
+        st[hlf] = va[hlf] && is_segment_start(seg, p, row_start);
+    }
+    const unsigned long long sm = (unsigned long long)__ballot_sync(0xffffffffu, st[0]) |
+                                  ((unsigned long long)__ballot_sync(0xffffffffu, st[1]) << 32);
+    const unsigned long long vm = (unsigned long long)__ballot_sync(0xffffffffu, va[0]) |
+                                  ((unsigned long long)__ballot_sync(0xffffffffu, va[1]) << 32);
+    if (lane == 0) {
+        pl.meta[c].start = sm;
+        pl.meta[c].valid = vm;
+        const unsigned long long cut = sm | ~vm;
+        pl.first_cut[c] = cut ? (__ffsll((long long)cut) - 1) : C;
+    }
+}
+
+constexpr int kChainThreads = 1024;
+
+__device__ int chain_scan(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = s_warp[lane];
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += n;
+        }
+        s_warp[lane] = wi - w;
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    const int r = s_warp[warp] + incl - v;
+    __syncthreads();
+    return r;
+}
+
+// Chains: a chain begins at chunk 0 and at every chunk holding a start or padding, and ends
+// before the next such chunk; no state crosses a chain's first chunk's last cut backwards or
+// its end forwards except through the chunk that ends it. Ordered longest first (counting sort,
+// lengths >= 1024 share a bucket). One CTA.
+__global__ void __launch_bounds__(kChainThreads, 1)
+bwd_chains_kernel(int64_t n_chunks, void* ws) {
+    BPlan pl = bplan_view(ws, n_chunks, 0);
+    __shared__ int s_warp[32];
+    __shared__ int s_total;
+    __shared__ int hist[kChainThreads];
+    const int tid = threadIdx.x;
+    int base = 0;
+    for (int64_t c0 = 0; c0 < n_chunks; c0 += kChainThreads) {
+        const int64_t c = c0 + tid;
+        const int flag = (c < n_chunks && (c == 0 || pl.first_cut[c] < C)) ? 1 : 0;
+        const int off = chain_scan(flag, s_warp, &s_total);
+        if (flag) pl.chains[base + off].x = int(c);
+        base += s_total;
+        __syncthreads();
+    }
+    const int n = base;
+    for (int k = tid; k < n; k += kChainThreads)
+        pl.chains[k].y = (k + 1 < n) ? pl.chains[k + 1].x : int(n_chunks);
+    hist[tid] = 0;
+    __syncthreads();
+    auto bucket = [&](int k) {
+        const int2 ch = pl.chains[k];
+        const int len = min(ch.y - ch.x, kChainThreads);
+        return kChainThreads - len;                  // 0 = longest
+    };
+    for (int k = tid; k < n; k += kChainThreads) atomicAdd(&hist[bucket(k)], 1);
+    __syncthreads();
+    const int off = chain_scan(hist[tid], s_warp, &s_total);
+    hist[tid] = off;
+    __syncthreads();
+    for (int k = tid; k < n; k += kChainThreads) pl.order[atomicAdd(&hist[bucket(k)], 1)] = k;
+    if (tid == 0) {
+        pl.counters[0] = n;
+        pl.counters[1] = 0;
+        pl.counters[2] = 0;
+    }
+}
+
+// ---- the state scans ----------------------------------------------------------------------
+
+constexpr int kScanThreads = 320;
+constexpr uint32_t kSOffX = 0;              // x (k or q) -> X_lo
+constexpr uint32_t kSOffG = kTile;          // g -> X_hi
+constexpr uint32_t kSOffY = 2 * kTile;      // y (v or dO), exact
+constexpr uint32_t kSStage = 3 * kTile;
+constexpr uint32_t kSOffMisc = 2 * kSStage;
+// misc: barriers at 0, the TMEM base at 64, per stage s at 128 + 1024 s: the chunk's
+// descriptor (32 B), beta (float[64]) at +64 and P (float[128]) at +320
+constexpr uint32_t kSMiscStage = 128;
+constexpr uint32_t kScanSmem = kSOffMisc + kSMiscStage + 2 * 1024 + 1024;
+static_assert(2 * kScanSmem <= 232448, "two scan CTAs per SM");
+
+enum : int { kFirst = 1, kLast = 2, kPre = 4, kPost = 8, kEnd = 16 };
+
+struct SDesc {
+    int c, h, flags, lo, hi, slot_pre, slot_post, pad;
+};
+
+struct ScanParams {
+    const __nv_bfloat16* beta;
+    float scale;
+    int64_t N;
+    int32_t H;
+    int64_t n_chunks;
+    void* ws;
+    uint32_t* status;
+};
+
+// kRev = false: x = k, y = v, exports S_in; kRev = true: x = q, y = dO, exports D_end.
+template <bool kRev>
+__global__ void __launch_bounds__(kScanThreads, 2)
+scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_g,
+            const __grid_constant__ CUtensorMap map_y, const __grid_constant__ ScanParams prm) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* misc = sm + kSOffMisc;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
+    uint64_t* bFull = bars + 0;     // [2] TMA bytes + the descriptor
+    uint64_t* bProl = bars + 2;     // [2] X ready (4 prologue warps)
+    uint64_t* bEmpty = bars + 4;    // [2] the stage's MMAs done
+    uint64_t* bReady = bars + 6;    // the state is decayed (4 state warps)
+    uint64_t* bSdone = bars + 7;    // the chunk's MMAs done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 64);
+    auto stage_misc = [&](uint32_t s) { return misc + kSMiscStage + s * 1024; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = prm.H;
+    const int64_t n_chunks = prm.n_chunks;
+    BPlan pl = bplan_view(prm.ws, n_chunks, H);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bFull[s], 2);
+            mbar_init(&bProl[s], 4);
+            mbar_init(&bEmpty[s], 1);
+        }
+        mbar_init(bReady, 4);
+        mbar_init(bSdone, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 128);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_x);
+        tma_prefetch_desc(&map_g);
+        tma_prefetch_desc(&map_y);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool timed_out = false;
+
+    if (warp == 0) {
+        // ================= producer =================
+        const int n_items = pl.counters[0] * H;
+        uint32_t it = 0;
+        for (;;) {
+            int item = 0;
+            if (lane == 0) item = atomicAdd(&pl.counters[kRev ? 2 : 1], 1);
+            item = __shfl_sync(0xffffffffu, item, 0);
+            const bool done = item >= n_items;
+            int c_from = 0, cnt = 1, step = 1, h = 0;
+            int2 ch = make_int2(0, 0);
+            bool post = false;
+            if (!done) {
+                ch = pl.chains[pl.order[item / H]];
+                h = item % H;
+                if (!kRev) {
+                    c_from = ch.x;
+                    cnt = ch.y - ch.x;
+                    post = ch.y < n_chunks && pl.first_cut[ch.y] > 0;
+                } else {
+                    const bool head = ch.y < n_chunks && pl.first_cut[ch.y] > 0;
+                    c_from = head ? ch.y : ch.y - 1;
+                    cnt = c_from - ch.x;              // chunks c_from down to ch.x + 1
+                    step = -1;
+                    post = true;
+                }
+                if (cnt <= 0) continue;
+            }
+            for (int k = 0; k < cnt; ++k, ++it) {
+                const uint32_t s = it & 1;
+                const int c = c_from + step * k;
+                ChunkMeta meta = {0ull, 0ull};
+                __nv_bfloat16 braw[2] = {__float2bfloat16(0.f), __float2bfloat16(0.f)};
+                int fc = C;
+                if (!done) {
+                    meta = pl.meta[c];
+                    fc = pl.first_cut[c];
+                    if (!kRev) {
+#pragma unroll
+                        for (int r2 = 0; r2 < 2; ++r2) {
+                            const int64_t p = int64_t(c) * C + lane + 32 * r2;
+                            if (p < prm.N) braw[r2] = prm.beta[p * H + h];
+                        }
+                    }
+                }
+                if (!warp_wait(&bEmpty[s], ((it >> 1) & 1) ^ 1)) { timed_out = true; break; }
+                uint8_t* smc = stage_misc(s);
+                SDesc* d = reinterpret_cast<SDesc*>(smc);
+                uint64_t* bar = &bFull[s];
+                if (done) {
+                    if (lane == 0) {
+                        d->flags = kEnd;
+                        mbar_arrive(bar);
+                    }
+                } else {
+                    uint8_t* st = sm + s * kSStage;
+                    const int32_t y = int32_t(int64_t(c) * C);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar, 3 * kTile);
+#pragma unroll
+                        for (int p = 0; p < 2; ++p) {
+                            tma_load_2d(st + kSOffX + p * kPanel, &map_x, bar, h * D + p * 64, y);
+                            tma_load_2d(st + kSOffG + p * kPanel, &map_g, bar, h * D + p * 64, y);
+                            tma_load_2d(st + kSOffY + p * kPanel, &map_y, bar, h * D + p * 64, y);
+                        }
+                    }
+                    if (!kRev) {
+                        float* beta = reinterpret_cast<float*>(smc + 64);
+#pragma unroll
+                        for (int r2 = 0; r2 < 2; ++r2) {
+                            const int r = lane + 32 * r2;
+                            beta[r] = ((meta.valid >> r) & 1ull) ? __bfloat162float(braw[r2]) : 0.f;
+                        }
+                    }
+                    if (lane == 0) {
+                        SDesc f;
+                        f.c = c;
+                        f.h = h;
+                        f.flags = (k == 0 ? kFirst : kPre) | (k == cnt - 1 ? kLast : 0) |
+                                  ((k == cnt - 1 && post) ? kPost : 0);
+                        if (!kRev) {
+                            // the chain's first chunk: only the rows of the segment that reaches
+                            // its end (from its last start; none when its last row is padding)
+                            const int ls = meta.start ? 63 - __clzll((long long)meta.start) : 0;
+                            f.lo = (k == 0) ? (((meta.valid >> 63) & 1ull) ? ls : C) : 0;
+                            f.hi = C;
+                        } else {
+                            // the chunk that ends the chain: the rows before its first cut
+                            f.lo = 0;
+                            f.hi = (k == 0 && c == ch.y) ? fc : C;
+                        }
+                        f.slot_pre = c;
+                        f.slot_post = kRev ? ch.x : ch.y;
+                        f.pad = 0;
+                        *d = f;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar);
+                __syncwarp();
+                if (done) break;
+            }
+            if (done || timed_out) break;
+        }
+        if (timed_out) set_status(prm.status, KDA_DEV_TIMEOUT);
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        const uint32_t sm_addr = smem_u32(sm);
+        for (uint32_t it = 0;; ++it) {
+            const uint32_t s = it & 1, ph = (it >> 1) & 1;
+            if (!warp_wait(&bFull[s], ph)) { timed_out = true; break; }
+            const SDesc f = *reinterpret_cast<const SDesc*>(stage_misc(s));
+            if (f.flags & kEnd) break;
+            if (!warp_wait(&bProl[s], ph)) { timed_out = true; break; }
+            if (!warp_wait(bReady, it & 1)) { timed_out = true; break; }
+            tc_fence_after();
+            const uint32_t st_addr = sm_addr + s * kSStage;
+            // S^T (+)= Y^T X: A = Y^T (MN-major), B = X (MN-major), 16 token rows per step
+            const uint64_t dY = sdesc_sw128(st_addr + kSOffY, kPanel, 1024);
+            const uint64_t dXh = sdesc_sw128(st_addr + kSOffG, kPanel, 1024);
+            const uint64_t dXl = sdesc_sw128(st_addr + kSOffX, kPanel, 1024);
+            const uint32_t id = idesc_bf16_f32(128, 128, 1, 1);
+            const uint32_t acc0 = (f.flags & kFirst) ? 0u : 1u;
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+                mma_bf16(tmem, dY + uint64_t(kk * 128), dXh + uint64_t(kk * 128), id, kk > 0 ? 1u : acc0);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+                mma_bf16(tmem, dY + uint64_t(kk * 128), dXl + uint64_t(kk * 128), id, 1u);
+            mma_commit(bSdone);
+            mma_commit(&bEmpty[s]);
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ================= prologue: X = x exp(...) as hi/lo, P =================
+        const int ch = threadIdx.x - 64;            // key channel
+        for (uint32_t it = 0;; ++it) {
+            const uint32_t s = it & 1, ph = (it >> 1) & 1;
+            if (!warp_wait(&bFull[s], ph)) { timed_out = true; break; }
+            uint8_t* smc = stage_misc(s);
+            const SDesc f = *reinterpret_cast<const SDesc*>(smc);
+            if (f.flags & kEnd) break;
+            uint8_t* st = sm + s * kSStage;
+            float* P = reinterpret_cast<float*>(smc + 320);
+            if (!kRev) {
+                const float* beta = reinterpret_cast<const float*>(smc + 64);
+                float suf = 0.f;                      // base-2 log-decay of the rows after t
+#pragma unroll 4
+                for (int t = C - 1; t >= 0; --t) {
+                    const uint32_t o = eoff(t, ch);
+                    uint32_t hi = 0, lo = 0;
+                    if (t >= f.lo) {
+                        const float x = ld_bf(st + kSOffX, o) * beta[t] * ex2a(suf);
+                        split1(x, hi, lo);
+                        suf += ld_bf(st + kSOffG, o) * kLog2e;
+                    }
+                    st_bf(st + kSOffG, o, hi);
+                    st_bf(st + kSOffX, o, lo);
+                }
+                P[ch] = ex2a(suf);
+            } else {
+                float gs = 0.f;                       // base-2 log-decay of rows 0..t
+#pragma unroll 4
+                for (int t = 0; t < C; ++t) {
+                    const uint32_t o = eoff(t, ch);
+                    uint32_t hi = 0, lo = 0;
+                    if (t < f.hi) {
+                        gs += ld_bf(st + kSOffG, o) * kLog2e;
+                        const float x = prm.scale * ld_bf(st + kSOffX, o) * ex2a(gs);
+                        split1(x, hi, lo);
+                    }
+                    st_bf(st + kSOffG, o, hi);
+                    st_bf(st + kSOffX, o, lo);
+                }
+                P[ch] = ex2a(gs);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bProl[s]);
+        }
+    } else {
+        // ================= state: export, decay =================
+        const int qd = warp & 3;                    // TMEM lane quarter
+        const int v = qd * 32 + lane;               // value channel (TMEM lane)
+        const uint32_t tl = tmem + (uint32_t(qd * 32) << 16);
+        float* const base = kRev ? pl.d_end : pl.s_in;
+        uint32_t nd = 0;                            // MMA completions waited for
+        for (uint32_t it = 0;; ++it) {
+            const uint32_t s = it & 1, ph = (it >> 1) & 1;
+            if (!warp_wait(&bFull[s], ph)) { timed_out = true; break; }
+            uint8_t* smc = stage_misc(s);
+            const SDesc f = *reinterpret_cast<const SDesc*>(smc);
+            if (f.flags & kEnd) break;
+            if (!(f.flags & kFirst)) {
+                if (!warp_wait(bSdone, nd & 1)) { timed_out = true; break; }
+                ++nd;
+                if (!warp_wait(&bProl[s], ph)) { timed_out = true; break; }
+                tc_fence_after();
+                const float* P = reinterpret_cast<const float*>(smc + 320);
+                float* dst = base + (size_t(f.slot_pre) * H + f.h) * (D * D) + v;
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(tl + cb * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float x = __uint_as_float(r[j]);
+                        __stcg(dst + (cb * 32 + j) * D, x);
+                        r[j] = __float_as_uint(x * P[cb * 32 + j]);
+                    }
+                    tmem_st32(tl + cb * 32, r);
+                }
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bReady);
+            if (f.flags & kLast) {
+                if (!warp_wait(bSdone, nd & 1)) { timed_out = true; break; }
+                ++nd;
+                tc_fence_after();
+                if (f.flags & kPost) {
+                    float* dst = base + (size_t(f.slot_post) * H + f.h) * (D * D) + v;
+#pragma unroll 1
+                    for (int cb = 0; cb < 4; ++cb) {
+                        uint32_t r[32];
+                        tmem_ld32(tl + cb * 32, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) __stcg(dst + (cb * 32 + j) * D, __uint_as_float(r[j]));
+                    }
+                }
+                tc_fence_before();
+            }
+        }
+    }
+    if (timed_out && lane == 0) set_status(prm.status, KDA_DEV_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+// ---- the gradient kernel ----------------------------------------------------------------
+
+constexpr int kGradThreads = 320;
+constexpr uint32_t kGK = 0;                   // k (exact), then with g: S_dec_lo
+constexpr uint32_t kGG = 1 * kTile;           // g (exact)
+constexpr uint32_t kGQL = 2 * kTile;          // q -> Qt_lo
+constexpr uint32_t kGQH = 3 * kTile;          // Qt_hi
+constexpr uint32_t kGKH = 4 * kTile;          // Ktb_hi
+constexpr uint32_t kGKL = 5 * kTile;          // Ktb_lo
+constexpr uint32_t kGV = 6 * kTile;           // v (exact); the epilogue's dbeta terms after
+constexpr uint32_t kGDO = 7 * kTile;          // dO (exact)
+constexpr uint32_t kGAH = 8 * kTile;          // A'_hi, 64 x 64 (8 KB); before it, with A'_lo,
+                                              // W_hi and W_lo: D_end_lo
+constexpr uint32_t kGAL = kGAH + C * C * 2;   // A'_lo
+constexpr uint32_t kGWH = kGAL + C * C * 2;   // W_hi
+constexpr uint32_t kGWL = kGWH + C * C * 2;   // W_lo
+constexpr uint32_t kGSD = kGWL + C * C * 2;   // S_dec_hi, 128 x 128 (32 KB)
+constexpr uint32_t kGDE = kGSD + kTile128;    // D_end_hi
+constexpr uint32_t kGSDL = kGK;               // S_dec_lo (over k and g)
+constexpr uint32_t kGDEL = kGAH;              // D_end_lo (over A' and W)
+constexpr uint32_t kGMisc = kGDE + kTile128;
+// misc: barriers at 0, the TMEM base at 64, beta (float[64]) at 128, P (float[128]) at 384,
+// the carried-state products (float[128]) at 896
+constexpr uint32_t kGMiscBytes = 1408;
+constexpr uint32_t kGradSmem = kGMisc + kGMiscBytes + 1024;
+static_assert(kGradSmem <= 232448, "shared memory per CTA");
+
+// tensor memory (columns)
+constexpr uint32_t kTmSC = 0;      // SC, M=64 layout (row t in lane 32 (t/16) + t%16)
+constexpr uint32_t kTmW = 64;      // W, M=64 layout
+constexpr uint32_t kTmQs = 128;    // Qs^T  (lane = key channel, column = token)
+constexpr uint32_t kTmT2 = 192;    // T2^T  (key channel)
+constexpr uint32_t kTmVs = 256;    // Vs^T  (value channel)
+constexpr uint32_t kTmQ = 320;     // dQ^T  (key channel)
+constexpr uint32_t kTmK = 384;     // dK^T  (key channel)
+constexpr uint32_t kTmV = 448;     // dV^T  (value channel)
+
+struct GradParams {
+    const __nv_bfloat16* k;          // read again by the epilogue (from L2)
+    const __nv_bfloat16* g;
+    const __nv_bfloat16* beta;
+    float scale;
+    int64_t N;
+    int32_t H;
+    int64_t n_chunks;
+    void* ws;
+    void* dq;
+    void* dk;
+    void* dv;
+    void* dg;
+    void* dbeta;
+    uint32_t* status;
+};
+
+template <typename To>
+__device__ __forceinline__ void store_out(void* base, size_t idx, float x) {
+    static_cast<To*>(base)[idx] = from_f32<To>(x);
+}
+
+// mask(SC or W) x mult as hi/lo bf16 tiles (K-major, 64 x 64), by one epilogue warp on its
+// TMEM lane quarter (rows 16 qd .. 16 qd + 15 of the M=64 accumulator): 16x256b loads give each
+// thread rows i0 = 16 qd + lane/4 and i0 + 8 at column pairs 8 r + 2 (lane % 4); stmatrix
+// writes the 8x8 blocks.
+__device__ __forceinline__ void mask_tiles(uint32_t taddr, uint8_t* t_hi, uint8_t* t_lo,
+                                           unsigned long long start, unsigned long long valid,
+                                           float mult, int qd, int lane) {
+    uint32_t r[32];
+    tmem_ld16x256b_x8(taddr, r);
+    tmem_ld_wait();
+    const int i0 = qd * 16 + (lane >> 2);
+    const int sh = 2 * (lane & 3);
+    const unsigned long long k0 = keep_bits(start, valid, i0) >> sh;
+    const unsigned long long k1 = keep_bits(start, valid, i0 + 8) >> sh;
+    uint32_t h0[8], l0[8], h1[8], l1[8];
+#pragma unroll
+    for (int rp = 0; rp < 8; ++rp) {
+        const float a0 = ((k0 >> (8 * rp)) & 1ull) ? mult * __uint_as_float(r[4 * rp]) : 0.f;
+        const float b0 = ((k0 >> (8 * rp + 1)) & 1ull) ? mult * __uint_as_float(r[4 * rp + 1]) : 0.f;
+        const float a1 = ((k1 >> (8 * rp)) & 1ull) ? mult * __uint_as_float(r[4 * rp + 2]) : 0.f;
+        const float b1 = ((k1 >> (8 * rp + 1)) & 1ull) ? mult * __uint_as_float(r[4 * rp + 3]) : 0.f;
+        split2(a0, b0, h0[rp], l0[rp]);
+        split2(a1, b1, h1[rp], l1[rp]);
+    }
+    const int mrow = qd * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+    const uint32_t a_hi = smem_u32(t_hi), a_lo = smem_u32(t_lo);
+#pragma unroll
+    for (int rp = 0; rp < 8; rp += 2) {
+        const int jc = rp + (lane >> 4);
+        const uint32_t off = (mrow >> 3) * 1024 + (mrow & 7) * 128 + ((jc ^ (mrow & 7)) << 4);
+        stmatrix_x4(a_hi + off, h0[rp], h1[rp], h0[rp + 1], h1[rp + 1]);
+        stmatrix_x4(a_lo + off, l0[rp], l1[rp], l0[rp + 1], l1[rp + 1]);
+    }
+}
+
+template <typename To>
+__global__ void __launch_bounds__(kGradThreads, 1)
+grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+            const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_v,
+            const __grid_constant__ CUtensorMap map_do, const __grid_constant__ GradParams prm) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* misc = sm + kGMisc;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
+    uint64_t* bFull = bars + 0;      // TMA bytes + beta
+    uint64_t* bProl = bars + 1;      // Qt, Ktb, P (4 prologue warps)
+    uint64_t* bConv = bars + 2;      // S_dec, D_end tiles (4 warps)
+    uint64_t* bScores = bars + 3;    // SC and W in TMEM
+    uint64_t* bMasked = bars + 4;    // A' and W tiles (4 warps)
+    uint64_t* bDone = bars + 5;      // all MMAs done
+    uint64_t* bEmpty = bars + 6;     // the epilogue has finished with the item (4 warps)
+    uint64_t* bStates = bars + 7;    // the products reading S_dec and D_end done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 64);
+    float* s_beta = reinterpret_cast<float*>(misc + 128);
+    float* s_P = reinterpret_cast<float*>(misc + 384);
+    float* s_rd = reinterpret_cast<float*>(misc + 896);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = prm.H;
+    const int64_t n_chunks = prm.n_chunks;
+    const int64_t n_items = n_chunks * H;
+    BPlan pl = bplan_view(prm.ws, n_chunks, H);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bFull, 2);
+        mbar_init(bProl, 4);
+        mbar_init(bConv, 4);
+        mbar_init(bScores, 1);
+        mbar_init(bMasked, 4);
+        mbar_init(bDone, 1);
+        mbar_init(bEmpty, 4);
+        mbar_init(bStates, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_k);
+        tma_prefetch_desc(&map_g);
+        tma_prefetch_desc(&map_v);
+        tma_prefetch_desc(&map_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool timed_out = false;
+
+    if (warp == 0) {
+        // ================= producer =================
+        uint32_t n = 0;
+        for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+            const int c = int(item / H), h = int(item % H);
+            const unsigned long long valid = pl.meta[c].valid;
+            __nv_bfloat16 braw[2] = {__float2bfloat16(0.f), __float2bfloat16(0.f)};
+#pragma unroll
+            for (int r2 = 0; r2 < 2; ++r2) {
+                const int64_t p = int64_t(c) * C + lane + 32 * r2;
+                if (p < prm.N) braw[r2] = prm.beta[p * H + h];
+            }
+            if (!warp_wait(bEmpty, (n & 1) ^ 1)) { timed_out = true; break; }
+            const int32_t y = int32_t(int64_t(c) * C);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bFull, 5 * kTile);
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int32_t x = h * D + p * 64;
+                    tma_load_2d(sm + kGK + p * kPanel, &map_k, bFull, x, y);
+                    tma_load_2d(sm + kGG + p * kPanel, &map_g, bFull, x, y);
+                    tma_load_2d(sm + kGQL + p * kPanel, &map_q, bFull, x, y);
+                    tma_load_2d(sm + kGV + p * kPanel, &map_v, bFull, x, y);
+                    tma_load_2d(sm + kGDO + p * kPanel, &map_do, bFull, x, y);
+                }
+            }
+#pragma unroll
+            for (int r2 = 0; r2 < 2; ++r2) {
+                const int r = lane + 32 * r2;
+                s_beta[r] = ((valid >> r) & 1ull) ? __bfloat162float(braw[r2]) : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bFull);
+            __syncwarp();
+        }
+        // copies still in flight when a wait gave up: wait for them (bounded) before exiting
+        if (timed_out && n > 0) (void)warp_wait(bFull, (n - 1) & 1);
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        const uint32_t a = smem_u32(sm);
+        const uint64_t dK_H = sdesc_sw128(a + kGKH, 16, 1024), dK_L = sdesc_sw128(a + kGKL, 16, 1024);
+        const uint64_t dQ_H = sdesc_sw128(a + kGQH, 16, 1024), dQ_L = sdesc_sw128(a + kGQL, 16, 1024);
+        const uint64_t dDO = sdesc_sw128(a + kGDO, 16, 1024), dV = sdesc_sw128(a + kGV, 16, 1024);
+        const uint64_t dSD = sdesc_sw128(a + kGSD, 16, 1024), dDE = sdesc_sw128(a + kGDE, 16, 1024);
+        const uint64_t dSDL = sdesc_sw128(a + kGSDL, 16, 1024), dDEL = sdesc_sw128(a + kGDEL, 16, 1024);
+        const uint64_t mDE = sdesc_sw128(a + kGDE, kPanel128, 1024);      // D_end^T (MN-major)
+        const uint64_t mDEL = sdesc_sw128(a + kGDEL, kPanel128, 1024);
+        const uint64_t mK_H = sdesc_sw128(a + kGKH, kPanel, 1024), mK_L = sdesc_sw128(a + kGKL, kPanel, 1024);
+        const uint64_t mQ_H = sdesc_sw128(a + kGQH, kPanel, 1024), mQ_L = sdesc_sw128(a + kGQL, kPanel, 1024);
+        const uint64_t mDO = sdesc_sw128(a + kGDO, kPanel, 1024);
+        const uint64_t dW_H = sdesc_sw128(a + kGWH, 16, 1024), dW_L = sdesc_sw128(a + kGWL, 16, 1024);
+        const uint64_t mW_H = sdesc_sw128(a + kGWH, kPanel, 1024), mW_L = sdesc_sw128(a + kGWL, kPanel, 1024);
+        const uint64_t mA_H = sdesc_sw128(a + kGAH, kPanel, 1024), mA_L = sdesc_sw128(a + kGAL, kPanel, 1024);
+        const uint32_t id64 = idesc_bf16_f32(64, 64, 0, 0);
+        const uint32_t idKK = idesc_bf16_f32(128, 64, 0, 0);
+        const uint32_t idMK = idesc_bf16_f32(128, 64, 1, 0);
+        const uint32_t idMM = idesc_bf16_f32(128, 64, 1, 1);
+        uint32_t n = 0;
+        for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+            const int c = int(item / H);
+            const int fc = pl.first_cut[c];
+            const bool cin = fc > 0;
+            const bool cout = (c + 1 < n_chunks) && pl.first_cut[c + 1] > 0;
+            const uint32_t ph = n & 1;
+            if (!warp_wait(bFull, ph)) { timed_out = true; break; }
+            tc_fence_after();
+            // W = dO V^T
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                mma_bf16(tmem + kTmW, dDO + kofs64(kk), dV + kofs64(kk), id64, kk > 0 ? 1u : 0u);
+            if (!warp_wait(bProl, ph)) { timed_out = true; break; }
+            tc_fence_after();
+            // SC = Qt Ktb^T as hi*hi + hi*lo + lo*hi
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                mma_bf16(tmem + kTmSC, dQ_H + kofs64(kk), dK_H + kofs64(kk), id64, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                mma_bf16(tmem + kTmSC, dQ_H + kofs64(kk), dK_L + kofs64(kk), id64, 1u);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                mma_bf16(tmem + kTmSC, dQ_L + kofs64(kk), dK_H + kofs64(kk), id64, 1u);
+            mma_commit(bScores);
+            if (!warp_wait(bConv, ph)) { timed_out = true; break; }
+            tc_fence_after();
+            if (cin) {           // Qs^T = S_dec dO^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16(tmem + kTmQs, dSD + kofs128(kk), dDO + kofs64(kk), idKK, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16(tmem + kTmQs, dSDL + kofs128(kk), dDO + kofs64(kk), idKK, 1u);
+            }
+            if (cout) {          // T2^T = D_end V^T;  Vs^T = D_end^T Ktb^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16(tmem + kTmT2, dDE + kofs128(kk), dV + kofs64(kk), idKK, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16(tmem + kTmT2, dDEL + kofs128(kk), dV + kofs64(kk), idKK, 1u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16(tmem + kTmVs, mDE + uint64_t(kk * 128), dK_H + kofs64(kk), idMK, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16(tmem + kTmVs, mDE + uint64_t(kk * 128), dK_L + kofs64(kk), idMK, 1u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16(tmem + kTmVs, mDEL + uint64_t(kk * 128), dK_H + kofs64(kk), idMK, 1u);
+            }
+            mma_commit(bStates);     // D_end_lo's space is the A' and W tiles'
+            if (!warp_wait(bMasked, ph)) { timed_out = true; break; }
+            tc_fence_after();
+            // dQ^T = Ktb^T W^T  (K = 64 tokens s; W^T's K-major rows are W's rows)
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+                mma_bf16(tmem + kTmQ, mK_H + uint64_t(kk * 128), dW_H + uint64_t(kk * 2), idMK, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+                mma_bf16(tmem + kTmQ, mK_H + uint64_t(kk * 128), dW_L + uint64_t(kk * 2), idMK, 1u);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+                mma_bf16(tmem + kTmQ, mK_L + uint64_t(kk * 128), dW_H + uint64_t(kk * 2), idMK, 1u);
+            // dK^T = Qt^T W  (K = 64 tokens t)
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+                mma_bf16(tmem + kTmK, mQ_H + uint64_t(kk * 128), mW_H + uint64_t(kk * 128), idMM, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+                mma_bf16(tmem + kTmK, mQ_H + uint64_t(kk * 128), mW_L + uint64_t(kk * 128), idMM, 1u);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+                mma_bf16(tmem + kTmK, mQ_L + uint64_t(kk * 128), mW_H + uint64_t(kk * 128), idMM, 1u);
+            // dV^T = dO^T A'  (K = 64 tokens t)
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+                mma_bf16(tmem + kTmV, mDO + uint64_t(kk * 128), mA_H + uint64_t(kk * 128), idMM, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+                mma_bf16(tmem + kTmV, mDO + uint64_t(kk * 128), mA_L + uint64_t(kk * 128), idMM, 1u);
+            mma_commit(bDone);
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ================= prologue: Qt, Ktb (hi/lo), P =================
+        const int ch = threadIdx.x - 64;
+        uint32_t n = 0;
+        for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+            const int c = int(item / H);
+            const unsigned long long valid = pl.meta[c].valid;
+            if (!warp_wait(bFull, n & 1)) { timed_out = true; break; }
+            float suf = 0.f;                       // base-2 log-decay of the real rows after t
+#pragma unroll 4
+            for (int t = C - 1; t >= 0; --t) {
+                const uint32_t o = eoff(t, ch);
+                uint32_t qh = 0, ql = 0, kh = 0, kl = 0;
+                if ((valid >> t) & 1ull) {
+                    const float qv = ld_bf(sm + kGQL, o), kv = ld_bf(sm + kGK, o);
+                    split1(qv * ex2a(-suf), qh, ql);
+                    split1(kv * s_beta[t] * ex2a(suf), kh, kl);
+                    suf += ld_bf(sm + kGG, o) * kLog2e;
+                }
+                st_bf(sm + kGQH, o, qh);
+                st_bf(sm + kGQL, o, ql);
+                st_bf(sm + kGKH, o, kh);
+                st_bf(sm + kGKL, o, kl);
+            }
+            s_P[ch] = ex2a(suf);
+            const bool out_of_range = __any_sync(0xffffffffu, suf < kRangeLog2);
+            if (out_of_range && lane == 0) set_status(prm.status, KDA_DEV_DECAY_RANGE);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bProl);
+        }
+    } else {
+        // ================= states, A' and W tiles, epilogue =================
+        const int qd = warp & 3;                 // TMEM lane quarter
+        const int wr = warp - 6;                 // rows of the state tiles: 32 wr ..
+        const int i = qd * 32 + lane;            // channel of this thread in the epilogue
+        const uint32_t tl = tmem + (uint32_t(qd * 32) << 16);
+        float* s_db = reinterpret_cast<float*>(sm + kGV);    // [64][128] dbeta terms
+        uint32_t n = 0;
+        for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+            const int c = int(item / H), h = int(item % H);
+            const ChunkMeta meta = pl.meta[c];
+            const int fc = pl.first_cut[c];
+            const bool cin = fc > 0;
+            const bool cout = (c + 1 < n_chunks) && pl.first_cut[c + 1] > 0;
+            const bool nocut = fc == C;
+            const int lo_last = meta.start ? 63 - __clzll((long long)meta.start) : 0;
+            const uint32_t ph = n & 1;
+
+            // ---- S_dec = diag(P) S_in and D_end as bf16 tiles; rowdot(S_in, D_end) ----
+            {
+                const float* src_s = pl.s_in + (size_t(c) * H + h) * (D * D);
+                const float* src_d = pl.d_end + (size_t(c) * H + h) * (D * D);
+                if (!warp_wait(bProl, ph)) { timed_out = true; break; }
+                if (cin || cout) {
+#pragma unroll 1
+                    for (int rb = 0; rb < 32; rb += 4) {
+                        float4 sv[4], dv4[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int r = wr * 32 + rb + u;
+                            sv[u] = cin ? __ldcs(reinterpret_cast<const float4*>(src_s + r * D) + lane)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                            dv4[u] = cout ? __ldcs(reinterpret_cast<const float4*>(src_d + r * D) + lane)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int r = wr * 32 + rb + u;
+                            const uint32_t off = eoff128(r, 4 * lane);
+                            if (cin) {
+                                const float p = s_P[r];
+                                uint2 wh, wl;
+                                split2(p * sv[u].x, p * sv[u].y, wh.x, wl.x);
+                                split2(p * sv[u].z, p * sv[u].w, wh.y, wl.y);
+                                *reinterpret_cast<uint2*>(sm + kGSD + off) = wh;
+                                *reinterpret_cast<uint2*>(sm + kGSDL + off) = wl;
+                            }
+                            if (cout) {
+                                uint2 wh, wl;
+                                split2(dv4[u].x, dv4[u].y, wh.x, wl.x);
+                                split2(dv4[u].z, dv4[u].w, wh.y, wl.y);
+                                *reinterpret_cast<uint2*>(sm + kGDE + off) = wh;
+                                *reinterpret_cast<uint2*>(sm + kGDEL + off) = wl;
+                                if (nocut) {
+                                    float dot = sv[u].x * dv4[u].x + sv[u].y * dv4[u].y +
+                                                sv[u].z * dv4[u].z + sv[u].w * dv4[u].w;
+#pragma unroll
+                                    for (int m = 16; m > 0; m >>= 1)
+                                        dot += __shfl_xor_sync(0xffffffffu, dot, m);
+                                    if (lane == 0) s_rd[r] = dot;
+                                }
+                            }
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bConv);
+            }
+            // ---- A' = scale mask(SC), W = mask(W) as hi/lo tiles (over D_end_lo, once read) ----
+            if (!warp_wait(bScores, ph)) { timed_out = true; break; }
+            if (!warp_wait(bStates, ph)) { timed_out = true; break; }
+            tc_fence_after();
+            mask_tiles(tl + kTmSC, sm + kGAH, sm + kGAL, meta.start, meta.valid, prm.scale, qd, lane);
+            mask_tiles(tl + kTmW, sm + kGWH, sm + kGWL, meta.start, meta.valid, 1.f, qd, lane);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bMasked);
+
+            // ---- epilogue ----
+            if (!warp_wait(bDone, ph)) { timed_out = true; break; }
+            tc_fence_after();
+            const float scale = prm.scale;
+            // the segment at the chunk's end goes on: dg's part past the chunk,
+            // rowdot(S_out, D_end) = [no cut] P rowdot(S_in, D_end) + sum_s Ktb_s T2_s
+            float carry = 0.f;
+            if (cout) {
+                carry = nocut ? s_P[i] * s_rd[i] : 0.f;
+#pragma unroll 1
+                for (int blk = lo_last >> 4; blk < 4; ++blk) {
+                    uint32_t t2[16];
+                    tmem_ld16(tl + kTmT2 + blk * 16, t2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int s = blk * 16 + j;
+                        if (s >= lo_last) {
+                            const uint32_t o = eoff(s, i);
+                            const float kt = ld_bf(sm + kGKH, o) + ld_bf(sm + kGKL, o);
+                            carry = fmaf(kt, __uint_as_float(t2[j]), carry);
+                        }
+                    }
+                }
+            }
+            float run = carry;
+            float suf = 0.f;
+            const size_t row_stride = size_t(H) * D;
+#pragma unroll 1
+            for (int blk = 7; blk >= 0; --blk) {
+                // k and g of this thread's channel for the block's 8 tokens (their tiles now
+                // hold S_dec_lo)
+                __nv_bfloat16 kb[8], gb[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int64_t p = int64_t(c) * C + blk * 8 + j;
+                    const size_t idx = size_t(p < prm.N ? p : 0) * row_stride + size_t(h) * D + i;
+                    kb[j] = prm.k[idx];
+                    gb[j] = prm.g[idx];
+                }
+                uint32_t aQ[8], aQs[8], aK[8], aT2[8], aV[8], aVs[8];
+                tmem_ld8(tl + kTmQ + blk * 8, aQ);
+                tmem_ld8(tl + kTmQs + blk * 8, aQs);
+                tmem_ld8(tl + kTmK + blk * 8, aK);
+                tmem_ld8(tl + kTmT2 + blk * 8, aT2);
+                tmem_ld8(tl + kTmV + blk * 8, aV);
+                tmem_ld8(tl + kTmVs + blk * 8, aVs);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 7; j >= 0; --j) {
+                    const int t = blk * 8 + j;
+                    const int64_t p = int64_t(c) * C + t;
+                    const uint32_t o = eoff(t, i);
+                    float dq = 0.f, dk = 0.f, dv = 0.f, dg = 0.f, db = 0.f;
+                    if ((meta.valid >> t) & 1ull) {
+                        const bool carried = t < fc;
+                        const bool last = cout && t >= lo_last;
+                        const float qsum = __uint_as_float(aQ[j]) + (carried ? __uint_as_float(aQs[j]) : 0.f);
+                        const float ksum = scale * __uint_as_float(aK[j]) + (last ? __uint_as_float(aT2[j]) : 0.f);
+                        const float eS = ex2a(suf);
+                        dq = scale * ex2a(-suf) * qsum;
+                        const float dkr = eS * ksum;
+                        dk = s_beta[t] * dkr;
+                        dv = __uint_as_float(aV[j]) + (last ? __uint_as_float(aVs[j]) : 0.f);
+                        db = __bfloat162float(kb[j]) * dkr;
+                        const float qt = ld_bf(sm + kGQH, o) + ld_bf(sm + kGQL, o);
+                        const float kt = ld_bf(sm + kGKH, o) + ld_bf(sm + kGKL, o);
+                        run += scale * qt * qsum - kt * ksum;
+                        const bool is_start = (meta.start >> t) & 1ull;
+                        dg = is_start ? 0.f : run;
+                        if (is_start) run = 0.f;
+                        suf += __bfloat162float(gb[j]) * kLog2e;
+                    } else {
+                        run = 0.f;
+                    }
+                    s_db[t * D + i] = db;
+                    if (p < prm.N) {
+                        const size_t idx = size_t(p) * row_stride + size_t(h) * D + i;
+                        store_out<To>(prm.dq, idx, dq);
+                        store_out<To>(prm.dk, idx, dk);
+                        store_out<To>(prm.dv, idx, dv);
+                        store_out<To>(prm.dg, idx, dg);
+                    }
+                }
+            }
+            tc_fence_before();
+            epi_sync();
+            // dbeta_t = sum over the 128 key channels, 16 rows per warp
+#pragma unroll 1
+            for (int tt = 0; tt < 16; ++tt) {
+                const int t = wr * 16 + tt;
+                const float4 x = reinterpret_cast<const float4*>(s_db + t * D)[lane];
+                float sum = (x.x + x.y) + (x.z + x.w);
+#pragma unroll
+                for (int m = 16; m > 0; m >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
+                const int64_t p = int64_t(c) * C + t;
+                if (lane == 0 && p < prm.N)
+                    store_out<To>(prm.dbeta, size_t(p) * H + h, sum);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bEmpty);
+        }
+    }
+    if (timed_out && lane == 0) set_status(prm.status, KDA_DEV_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace tcb
+
+size_t bwd_tc_workspace_bytes(int64_t N, int32_t H) {
+    const int64_t n_chunks = ceil_div(N, kChunk);
+    return tcb::bplan_bytes(n_chunks) + 2 * size_t(n_chunks) * H * tcb::kStateBytes;
+}
+
+kda_status_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* g,
+                           const void* beta, const void* d_o, const int32_t* seg, int64_t B,
+                           int64_t T_len, int32_t H, float scale, kda_dtype_t grad_dtype,
+                           void* dq, void* dk, void* dv, void* dg, void* dbeta, void* ws,
+                           uint32_t* status_dev, cudaStream_t stream) {
+    using namespace tcb;
+    const int64_t N = B * T_len;
+    const int64_t n_chunks = ceil_div(N, C);
+    CUtensorMap m[5];
+    if (!tc::make_map(&m[0], q, N, H) || !tc::make_map(&m[1], k, N, H) ||
+        !tc::make_map(&m[2], g, N, H) || !tc::make_map(&m[3], v, N, H) ||
+        !tc::make_map(&m[4], d_o, N, H))
+        return KDA_ERR_CUDA;
+    const int sms = max(1, sm_count());
+    bwd_masks_kernel<<<unsigned(ceil_div(n_chunks, 8)), 256, 0, stream>>>(
+        seg, N, RowStartTest::make(T_len), n_chunks, ws);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    bwd_chains_kernel<<<1, kChainThreads, 0, stream>>>(n_chunks, ws);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    if (dynamic_smem_attr<scan_kernel<false>>(int(kScanSmem)) != cudaSuccess ||
+        dynamic_smem_attr<scan_kernel<true>>(int(kScanSmem)) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    ScanParams sp;
+    sp.beta = static_cast<const __nv_bfloat16*>(beta);
+    sp.scale = scale;
+    sp.N = N;
+    sp.H = H;
+    sp.n_chunks = n_chunks;
+    sp.ws = ws;
+    sp.status = status_dev;
+    const int64_t n_items = n_chunks * H;
+    const unsigned scan_grid = unsigned(n_items < 2 * sms ? n_items : 2 * sms);
+    scan_kernel<false><<<scan_grid, kScanThreads, kScanSmem, stream>>>(m[1], m[2], m[3], sp);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    scan_kernel<true><<<scan_grid, kScanThreads, kScanSmem, stream>>>(m[0], m[2], m[4], sp);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    GradParams gp;
+    gp.k = static_cast<const __nv_bfloat16*>(k);
+    gp.g = static_cast<const __nv_bfloat16*>(g);
+    gp.beta = sp.beta;
+    gp.scale = scale;
+    gp.N = N;
+    gp.H = H;
+    gp.n_chunks = n_chunks;
+    gp.ws = ws;
+    gp.dq = dq;
+    gp.dk = dk;
+    gp.dv = dv;
+    gp.dg = dg;
+    gp.dbeta = dbeta;
+    gp.status = status_dev;
+    const unsigned grid = unsigned(n_items < sms ? n_items : sms);
+    if (grad_dtype == KDA_F32) {
+        if (dynamic_smem_attr<grad_kernel<float>>(int(kGradSmem)) != cudaSuccess) return KDA_ERR_CUDA;
+        grad_kernel<float><<<grid, kGradThreads, kGradSmem, stream>>>(m[0], m[1], m[2], m[3], m[4], gp);
+    } else {
+        if (dynamic_smem_attr<grad_kernel<__nv_bfloat16>>(int(kGradSmem)) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        grad_kernel<__nv_bfloat16><<<grid, kGradThreads, kGradSmem, stream>>>(m[0], m[1], m[2], m[3],
+                                                                             m[4], gp);
+    }
+    return launch_status();
+}
+
+}  // namespace kda

@@ -1,9 +1,10 @@
-"""GPU parity for kda_chunk_bwd_varlen (gradients of the packed forward).
+"""GPU parity for kda_chunk_bwd_varlen's fp32 walks (method="walk").
 
-The backward runs in fp32 arithmetic from the stored inputs, so every gradient
-is held to the fp32 bound max|x - x_ref| <= 1e-4 RMS(x_ref) per head, over real
+The walks run in fp32 arithmetic from the stored inputs, so every gradient is
+held to the fp32 bound max|x - x_ref| <= 1e-4 RMS(x_ref) per head, over real
 tokens, for either input dtype; gradients stored in bf16 get half a bf16 ulp more
-for their rounding. Padding tokens get exact zeros.
+for their rounding. Padding tokens get exact zeros. The tensor-core path (the
+default for bf16 with 128-wide heads) is tested in test_gpu_bwd_tc.py.
 """
 import numpy as np
 import pytest
@@ -32,12 +33,12 @@ def _check(grads, refs, seg, heads=None, label=""):
         check_kda_output(got, ref, seg, torch.float32, heads=heads, label=f"{label} {name}")
 
 
-def _run(inp, B, T, d_o, scale=1.0, grad_dtype=None, seg="inputs", dev=None):
+def _run(inp, B, T, d_o, scale=1.0, grad_dtype=None, seg="inputs", dev=None, method="walk"):
     s = inp.segment_ids if seg == "inputs" else seg
     to = (lambda t: t.cuda()) if dev is None else (lambda t: t)
     out = kda.kda_chunk_bwd_varlen(to(inp.q), to(inp.k), to(inp.v), to(inp.g), to(inp.beta),
                                    to(d_o), None if s is None else to(s), scale=scale, B=B, T=T,
-                                   grad_dtype=grad_dtype)
+                                   grad_dtype=grad_dtype, method=method)
     torch.cuda.synchronize()
     return out
 

@@ -92,8 +92,9 @@ struct BPlan {
     int32_t* first_cut;    // [n_chunks] first start-or-padding row, 64 if none
     int2* chains;          // [n_chunks] (first chunk, chunk after the last)
     int32_t* order;        // [n_chunks] chains, longest first
-    float* s_in;           // [n_chunks][H][128][128] state entering the chunk (row = key channel)
-    float* d_end;          // [n_chunks][H][128][128] adjoint at the chunk's end (row = key channel)
+    float* s_in;           // [n_chunks][H] state entering the chunk, as hi and lo bf16 tiles
+    float* d_end;          // [n_chunks][H] adjoint at the chunk's end, likewise (each 2 x 32 KB:
+                           // 128 x 128, row = key channel, K-major 128B-swizzled)
 };
 
 __host__ __device__ inline size_t bplan_bytes(int64_t n_chunks) {
@@ -570,7 +571,16 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
         const int qd = warp & 3;                    // TMEM lane quarter
         const int v = qd * 32 + lane;               // value channel (TMEM lane)
         const uint32_t tl = tmem + (uint32_t(qd * 32) << 16);
-        float* const base = kRev ? pl.d_end : pl.s_in;
+        uint8_t* const base = reinterpret_cast<uint8_t*>(kRev ? pl.d_end : pl.s_in);
+        // the state as the gradient kernel's operand: hi and lo bf16 tiles, 128 x 128 K-major
+        // 128B-swizzled (row = key channel), element (key, v) at eoff128(key, v)
+        auto put = [&](uint8_t* tile, int key, float x) {
+            uint32_t hi, lo;
+            split1(x, hi, lo);
+            const uint32_t off = eoff128(key, v);
+            *reinterpret_cast<uint16_t*>(tile + off) = uint16_t(hi);
+            *reinterpret_cast<uint16_t*>(tile + kTile128 + off) = uint16_t(lo);
+        };
         uint32_t nd = 0;                            // MMA completions waited for
         for (uint32_t it = 0;; ++it) {
             const uint32_t s = it & 1, ph = (it >> 1) & 1;
@@ -584,7 +594,7 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
                 if (!warp_wait(&bProl[s], ph)) { timed_out = true; break; }
                 tc_fence_after();
                 const float* P = reinterpret_cast<const float*>(smc + 320);
-                float* dst = base + (size_t(f.slot_pre) * H + f.h) * (D * D) + v;
+                uint8_t* dst = base + (size_t(f.slot_pre) * H + f.h) * kStateBytes;
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t r[32];
@@ -593,7 +603,7 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const float x = __uint_as_float(r[j]);
-                        __stcg(dst + (cb * 32 + j) * D, x);
+                        put(dst, cb * 32 + j, x);
                         r[j] = __float_as_uint(x * P[cb * 32 + j]);
                     }
                     tmem_st32(tl + cb * 32, r);
@@ -608,14 +618,14 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
                 ++nd;
                 tc_fence_after();
                 if (f.flags & kPost) {
-                    float* dst = base + (size_t(f.slot_post) * H + f.h) * (D * D) + v;
+                    uint8_t* dst = base + (size_t(f.slot_post) * H + f.h) * kStateBytes;
 #pragma unroll 1
                     for (int cb = 0; cb < 4; ++cb) {
                         uint32_t r[32];
                         tmem_ld32(tl + cb * 32, r);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) __stcg(dst + (cb * 32 + j) * D, __uint_as_float(r[j]));
+                        for (int j = 0; j < 32; ++j) put(dst, cb * 32 + j, __uint_as_float(r[j]));
                     }
                 }
                 tc_fence_before();
@@ -634,27 +644,27 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
 // ---- the gradient kernel ----------------------------------------------------------------
 
 constexpr int kGradThreads = 320;
-constexpr uint32_t kGK = 0;                   // k (exact), then with g: S_dec_lo
+constexpr uint32_t kGK = 0;                   // k (exact), then with g: S_in_lo
 constexpr uint32_t kGG = 1 * kTile;           // g (exact)
 constexpr uint32_t kGQL = 2 * kTile;          // q -> Qt_lo
 constexpr uint32_t kGQH = 3 * kTile;          // Qt_hi
 constexpr uint32_t kGKH = 4 * kTile;          // Ktb_hi
 constexpr uint32_t kGKL = 5 * kTile;          // Ktb_lo
-constexpr uint32_t kGV = 6 * kTile;           // v (exact); the epilogue's dbeta terms after
+constexpr uint32_t kGV = 6 * kTile;           // v (exact)
 constexpr uint32_t kGDO = 7 * kTile;          // dO (exact)
 constexpr uint32_t kGAH = 8 * kTile;          // A'_hi, 64 x 64 (8 KB); before it, with A'_lo,
-                                              // W_hi and W_lo: D_end_lo
-constexpr uint32_t kGAL = kGAH + C * C * 2;   // A'_lo
+constexpr uint32_t kGAL = kGAH + C * C * 2;   //   W_hi and W_lo: D_end_lo
 constexpr uint32_t kGWH = kGAL + C * C * 2;   // W_hi
 constexpr uint32_t kGWL = kGWH + C * C * 2;   // W_lo
-constexpr uint32_t kGSD = kGWL + C * C * 2;   // S_dec_hi, 128 x 128 (32 KB)
-constexpr uint32_t kGDE = kGSD + kTile128;    // D_end_hi
-constexpr uint32_t kGSDL = kGK;               // S_dec_lo (over k and g)
-constexpr uint32_t kGDEL = kGAH;              // D_end_lo (over A' and W)
-constexpr uint32_t kGMisc = kGDE + kTile128;
-// misc: barriers at 0, the TMEM base at 64, beta (float[64]) at 128, P (float[128]) at 384,
-// the carried-state products (float[128]) at 896
-constexpr uint32_t kGMiscBytes = 1408;
+constexpr uint32_t kGSH = kGWL + C * C * 2;   // S_in_hi, 128 x 128 (32 KB)
+constexpr uint32_t kGDH = kGSH + kTile128;    // D_end_hi
+constexpr uint32_t kGSL = kGK;                // S_in_lo (over k and g)
+constexpr uint32_t kGDL = kGAH;               // D_end_lo (over A' and W)
+constexpr uint32_t kGMisc = kGDH + kTile128;
+// misc: barriers at 0, the TMEM base at 96, beta (float[64], the prologue's) at 128, P
+// (float[128]) at 384, dg's part past the chunk (float[128]) at 896, the epilogue warps'
+// dbeta partial sums (float[2][4][8], by block parity) at 1408
+constexpr uint32_t kGMiscBytes = 1664;
 constexpr uint32_t kGradSmem = kGMisc + kGMiscBytes + 1024;
 static_assert(kGradSmem <= 232448, "shared memory per CTA");
 
@@ -669,7 +679,8 @@ constexpr uint32_t kTmK = 384;     // dK^T  (key channel)
 constexpr uint32_t kTmV = 448;     // dV^T  (value channel)
 
 struct GradParams {
-    const __nv_bfloat16* k;          // read again by the epilogue (from L2)
+    const __nv_bfloat16* q;          // read again by the epilogue (from L2)
+    const __nv_bfloat16* k;
     const __nv_bfloat16* g;
     const __nv_bfloat16* beta;
     float scale;
@@ -690,10 +701,21 @@ __device__ __forceinline__ void store_out(void* base, size_t idx, float x) {
     static_cast<To*>(base)[idx] = from_f32<To>(x);
 }
 
-// mask(SC or W) x mult as hi/lo bf16 tiles (K-major, 64 x 64), by one epilogue warp on its
-// TMEM lane quarter (rows 16 qd .. 16 qd + 15 of the M=64 accumulator): 16x256b loads give each
-// thread rows i0 = 16 qd + lane/4 and i0 + 8 at column pairs 8 r + 2 (lane % 4); stmatrix
-// writes the 8x8 blocks.
+// Bulk copy (no tensor map) of `bytes` (a multiple of 16) from global to shared memory,
+// completion signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+          "r"(smem_u32(bar))
+        : "memory");
+}
+
+// mask(SC or W) x mult as hi/lo bf16 tiles (K-major, 64 x 64), by one warp on its TMEM lane
+// quarter (rows 16 qd .. 16 qd + 15 of the M=64 accumulator): 16x256b loads give each thread
+// rows i0 = 16 qd + lane/4 and i0 + 8 at column pairs 8 r + 2 (lane % 4); stmatrix writes the
+// 8x8 blocks.
 __device__ __forceinline__ void mask_tiles(uint32_t taddr, uint8_t* t_hi, uint8_t* t_lo,
                                            unsigned long long start, unsigned long long valid,
                                            float mult, int qd, int lane) {
@@ -725,6 +747,47 @@ __device__ __forceinline__ void mask_tiles(uint32_t taddr, uint8_t* t_hi, uint8_
     }
 }
 
+// Sum over a warp's 32 lanes of each of v[0..7]: a butterfly that halves the vector at each
+// exchange (9 shuffles). Lane l ends up with the sum for entry ((l >> 2) & 7) in lanes with
+// (l & 3) == 0.
+__device__ __forceinline__ float warp_sum8(float (&v)[8], int lane) {
+    float a[4];
+    {
+        const bool up = lane & 16;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float send = up ? v[e] : v[e + 4];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+            a[e] = (up ? v[e + 4] : v[e]) + recv;
+        }
+    }
+    float b[2];
+    {
+        const bool up = lane & 8;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float send = up ? a[e] : a[e + 2];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
+            b[e] = (up ? a[e + 2] : a[e]) + recv;
+        }
+    }
+    float x;
+    {
+        const bool up = lane & 4;
+        const float send = up ? b[0] : b[1];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 4);
+        x = (up ? b[1] : b[0]) + recv;
+    }
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x;
+}
+// entry of v that warp_sum8 leaves in lane l: bit 16 of l picks the upper half, bit 8 the
+// upper quarter, bit 4 the upper eighth
+__device__ __forceinline__ int warp_sum8_entry(int lane) {
+    return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+}
+
 template <typename To>
 __global__ void __launch_bounds__(kGradThreads, 1)
 grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -734,18 +797,20 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* misc = sm + kGMisc;
     uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
-    uint64_t* bFull = bars + 0;      // TMA bytes + beta
+    uint64_t* bFull = bars + 0;      // q, k, g, v, dO bytes + beta
     uint64_t* bProl = bars + 1;      // Qt, Ktb, P (4 prologue warps)
-    uint64_t* bConv = bars + 2;      // S_dec, D_end tiles (4 warps)
+    uint64_t* bSt = bars + 2;        // S_in and D_end tiles' bytes
     uint64_t* bScores = bars + 3;    // SC and W in TMEM
-    uint64_t* bMasked = bars + 4;    // A' and W tiles (4 warps)
-    uint64_t* bDone = bars + 5;      // all MMAs done
-    uint64_t* bEmpty = bars + 6;     // the epilogue has finished with the item (4 warps)
-    uint64_t* bStates = bars + 7;    // the products reading S_dec and D_end done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 64);
+    uint64_t* bStates = bars + 4;    // the products reading S_in and D_end done
+    uint64_t* bMasked = bars + 5;    // A' and W tiles, dg's part past the chunk (4 warps)
+    uint64_t* bDone = bars + 6;      // all products done: every tile is free
+    uint64_t* bTmemFree = bars + 7;  // the epilogue has read TMEM (4 warps)
+    uint64_t* bMiscFree = bars + 8;  // the epilogue has read P and the carry (4 warps)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 96);
     float* s_beta = reinterpret_cast<float*>(misc + 128);
     float* s_P = reinterpret_cast<float*>(misc + 384);
-    float* s_rd = reinterpret_cast<float*>(misc + 896);
+    float* s_carry = reinterpret_cast<float*>(misc + 896);
+    float* s_dbw = reinterpret_cast<float*>(misc + 1408);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = prm.H;
@@ -756,12 +821,13 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     if (threadIdx.x == 0) {
         mbar_init(bFull, 2);
         mbar_init(bProl, 4);
-        mbar_init(bConv, 4);
+        mbar_init(bSt, 1);
         mbar_init(bScores, 1);
+        mbar_init(bStates, 1);
         mbar_init(bMasked, 4);
         mbar_init(bDone, 1);
-        mbar_init(bEmpty, 4);
-        mbar_init(bStates, 1);
+        mbar_init(bTmemFree, 4);
+        mbar_init(bMiscFree, 4);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -787,14 +853,20 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
             const int c = int(item / H), h = int(item % H);
             const unsigned long long valid = pl.meta[c].valid;
+            const bool cin = pl.first_cut[c] > 0;
+            const bool cout = (c + 1 < n_chunks) && pl.first_cut[c + 1] > 0;
             __nv_bfloat16 braw[2] = {__float2bfloat16(0.f), __float2bfloat16(0.f)};
 #pragma unroll
             for (int r2 = 0; r2 < 2; ++r2) {
                 const int64_t p = int64_t(c) * C + lane + 32 * r2;
                 if (p < prm.N) braw[r2] = prm.beta[p * H + h];
             }
-            if (!warp_wait(bEmpty, (n & 1) ^ 1)) { timed_out = true; break; }
+            // every tile is free once the previous item's products are done (the epilogue
+            // reads only tensor memory and L2)
+            if (n > 0 && !warp_wait(bDone, (n - 1) & 1)) { timed_out = true; break; }
             const int32_t y = int32_t(int64_t(c) * C);
+            const uint8_t* st_s = reinterpret_cast<const uint8_t*>(pl.s_in) + (size_t(c) * H + h) * kStateBytes;
+            const uint8_t* st_d = reinterpret_cast<const uint8_t*>(pl.d_end) + (size_t(c) * H + h) * kStateBytes;
             if (lane == 0) {
                 mbar_arrive_expect_tx(bFull, 5 * kTile);
 #pragma unroll
@@ -806,6 +878,17 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                     tma_load_2d(sm + kGV + p * kPanel, &map_v, bFull, x, y);
                     tma_load_2d(sm + kGDO + p * kPanel, &map_do, bFull, x, y);
                 }
+                const uint32_t st_bytes = (cin ? 2 * kTile128 : 0u) + (cout ? 2 * kTile128 : 0u);
+                if (st_bytes) {
+                    mbar_arrive_expect_tx(bSt, st_bytes);
+                    if (cout) {
+                        bulk_load(sm + kGDH, st_d, kTile128, bSt);
+                        bulk_load(sm + kGDL, st_d + kTile128, kTile128, bSt);
+                    }
+                    if (cin) bulk_load(sm + kGSH, st_s, kTile128, bSt);
+                } else {
+                    mbar_arrive(bSt);
+                }
             }
 #pragma unroll
             for (int r2 = 0; r2 < 2; ++r2) {
@@ -814,20 +897,26 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bFull);
+            // S_in_lo goes over k and g once the prologue has read them
+            if (!warp_wait(bProl, n & 1)) { timed_out = true; break; }
+            if (lane == 0 && cin) bulk_load(sm + kGSL, st_s + kTile128, kTile128, bSt);
             __syncwarp();
         }
         // copies still in flight when a wait gave up: wait for them (bounded) before exiting
-        if (timed_out && n > 0) (void)warp_wait(bFull, (n - 1) & 1);
+        if (timed_out && n > 0) {
+            (void)warp_wait(bFull, (n - 1) & 1);
+            (void)warp_wait(bSt, (n - 1) & 1);
+        }
     } else if (warp == 1) {
         // ================= MMA issuer =================
         const uint32_t a = smem_u32(sm);
         const uint64_t dK_H = sdesc_sw128(a + kGKH, 16, 1024), dK_L = sdesc_sw128(a + kGKL, 16, 1024);
         const uint64_t dQ_H = sdesc_sw128(a + kGQH, 16, 1024), dQ_L = sdesc_sw128(a + kGQL, 16, 1024);
         const uint64_t dDO = sdesc_sw128(a + kGDO, 16, 1024), dV = sdesc_sw128(a + kGV, 16, 1024);
-        const uint64_t dSD = sdesc_sw128(a + kGSD, 16, 1024), dDE = sdesc_sw128(a + kGDE, 16, 1024);
-        const uint64_t dSDL = sdesc_sw128(a + kGSDL, 16, 1024), dDEL = sdesc_sw128(a + kGDEL, 16, 1024);
-        const uint64_t mDE = sdesc_sw128(a + kGDE, kPanel128, 1024);      // D_end^T (MN-major)
-        const uint64_t mDEL = sdesc_sw128(a + kGDEL, kPanel128, 1024);
+        const uint64_t dSH = sdesc_sw128(a + kGSH, 16, 1024), dSL = sdesc_sw128(a + kGSL, 16, 1024);
+        const uint64_t dDH = sdesc_sw128(a + kGDH, 16, 1024), dDL = sdesc_sw128(a + kGDL, 16, 1024);
+        const uint64_t mDH = sdesc_sw128(a + kGDH, kPanel128, 1024);      // D_end^T (MN-major)
+        const uint64_t mDL = sdesc_sw128(a + kGDL, kPanel128, 1024);
         const uint64_t mK_H = sdesc_sw128(a + kGKH, kPanel, 1024), mK_L = sdesc_sw128(a + kGKL, kPanel, 1024);
         const uint64_t mQ_H = sdesc_sw128(a + kGQH, kPanel, 1024), mQ_L = sdesc_sw128(a + kGQL, kPanel, 1024);
         const uint64_t mDO = sdesc_sw128(a + kGDO, kPanel, 1024);
@@ -841,13 +930,13 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         uint32_t n = 0;
         for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
             const int c = int(item / H);
-            const int fc = pl.first_cut[c];
-            const bool cin = fc > 0;
+            const bool cin = pl.first_cut[c] > 0;
             const bool cout = (c + 1 < n_chunks) && pl.first_cut[c + 1] > 0;
             const uint32_t ph = n & 1;
             if (!warp_wait(bFull, ph)) { timed_out = true; break; }
             tc_fence_after();
-            // W = dO V^T
+            // W = dO V^T (its TMEM columns are free: the previous item's masking read them
+            // before its last products)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
                 mma_bf16(tmem + kTmW, dDO + kofs64(kk), dV + kofs64(kk), id64, kk > 0 ? 1u : 0u);
@@ -864,32 +953,34 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             for (int kk = 0; kk < D / 16; ++kk)
                 mma_bf16(tmem + kTmSC, dQ_L + kofs64(kk), dK_H + kofs64(kk), id64, 1u);
             mma_commit(bScores);
-            if (!warp_wait(bConv, ph)) { timed_out = true; break; }
+            // the state products write columns the previous item's epilogue reads
+            if (!warp_wait(bSt, ph)) { timed_out = true; break; }
+            if (n > 0 && !warp_wait(bTmemFree, (n - 1) & 1)) { timed_out = true; break; }
             tc_fence_after();
-            if (cin) {           // Qs^T = S_dec dO^T
+            if (cin) {           // Qs^T = S_in dO^T (the decay P is applied in the epilogue)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmQs, dSD + kofs128(kk), dDO + kofs64(kk), idKK, kk > 0 ? 1u : 0u);
+                    mma_bf16(tmem + kTmQs, dSH + kofs128(kk), dDO + kofs64(kk), idKK, kk > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmQs, dSDL + kofs128(kk), dDO + kofs64(kk), idKK, 1u);
+                    mma_bf16(tmem + kTmQs, dSL + kofs128(kk), dDO + kofs64(kk), idKK, 1u);
             }
             if (cout) {          // T2^T = D_end V^T;  Vs^T = D_end^T Ktb^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmT2, dDE + kofs128(kk), dV + kofs64(kk), idKK, kk > 0 ? 1u : 0u);
+                    mma_bf16(tmem + kTmT2, dDH + kofs128(kk), dV + kofs64(kk), idKK, kk > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmT2, dDEL + kofs128(kk), dV + kofs64(kk), idKK, 1u);
+                    mma_bf16(tmem + kTmT2, dDL + kofs128(kk), dV + kofs64(kk), idKK, 1u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmVs, mDE + uint64_t(kk * 128), dK_H + kofs64(kk), idMK, kk > 0 ? 1u : 0u);
+                    mma_bf16(tmem + kTmVs, mDH + uint64_t(kk * 128), dK_H + kofs64(kk), idMK, kk > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmVs, mDE + uint64_t(kk * 128), dK_L + kofs64(kk), idMK, 1u);
+                    mma_bf16(tmem + kTmVs, mDH + uint64_t(kk * 128), dK_L + kofs64(kk), idMK, 1u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmVs, mDEL + uint64_t(kk * 128), dK_H + kofs64(kk), idMK, 1u);
+                    mma_bf16(tmem + kTmVs, mDL + uint64_t(kk * 128), dK_H + kofs64(kk), idMK, 1u);
             }
             mma_commit(bStates);     // D_end_lo's space is the A' and W tiles'
             if (!warp_wait(bMasked, ph)) { timed_out = true; break; }
@@ -925,19 +1016,25 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         }
         __syncwarp();
     } else if (warp < 6) {
-        // ================= prologue: Qt, Ktb (hi/lo), P =================
-        const int ch = threadIdx.x - 64;
+        // ================= prologue: Qt, Ktb (hi/lo), P; the A' and W tiles; the carry =======
+        const int qd = warp & 3;                 // TMEM lane quarter
+        const int ch = qd * 32 + lane;           // key channel (= TMEM lane of T2)
+        const uint32_t tl = tmem + (uint32_t(qd * 32) << 16);
         uint32_t n = 0;
         for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
             const int c = int(item / H);
-            const unsigned long long valid = pl.meta[c].valid;
-            if (!warp_wait(bFull, n & 1)) { timed_out = true; break; }
+            const ChunkMeta meta = pl.meta[c];
+            const int fc = pl.first_cut[c];
+            const bool cout = (c + 1 < n_chunks) && pl.first_cut[c + 1] > 0;
+            const int lo_last = meta.start ? 63 - __clzll((long long)meta.start) : 0;
+            const uint32_t ph = n & 1;
+            if (!warp_wait(bFull, ph)) { timed_out = true; break; }
             float suf = 0.f;                       // base-2 log-decay of the real rows after t
 #pragma unroll 4
             for (int t = C - 1; t >= 0; --t) {
                 const uint32_t o = eoff(t, ch);
                 uint32_t qh = 0, ql = 0, kh = 0, kl = 0;
-                if ((valid >> t) & 1ull) {
+                if ((meta.valid >> t) & 1ull) {
                     const float qv = ld_bf(sm + kGQL, o), kv = ld_bf(sm + kGK, o);
                     split1(qv * ex2a(-suf), qh, ql);
                     split1(kv * s_beta[t] * ex2a(suf), kh, kl);
@@ -948,133 +1045,132 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                 st_bf(sm + kGKH, o, kh);
                 st_bf(sm + kGKL, o, kl);
             }
-            s_P[ch] = ex2a(suf);
             const bool out_of_range = __any_sync(0xffffffffu, suf < kRangeLog2);
             if (out_of_range && lane == 0) set_status(prm.status, KDA_DEV_DECAY_RANGE);
+            const float Pch = ex2a(suf);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bProl);
-        }
-    } else {
-        // ================= states, A' and W tiles, epilogue =================
-        const int qd = warp & 3;                 // TMEM lane quarter
-        const int wr = warp - 6;                 // rows of the state tiles: 32 wr ..
-        const int i = qd * 32 + lane;            // channel of this thread in the epilogue
-        const uint32_t tl = tmem + (uint32_t(qd * 32) << 16);
-        float* s_db = reinterpret_cast<float*>(sm + kGV);    // [64][128] dbeta terms
-        uint32_t n = 0;
-        for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
-            const int c = int(item / H), h = int(item % H);
-            const ChunkMeta meta = pl.meta[c];
-            const int fc = pl.first_cut[c];
-            const bool cin = fc > 0;
-            const bool cout = (c + 1 < n_chunks) && pl.first_cut[c + 1] > 0;
-            const bool nocut = fc == C;
-            const int lo_last = meta.start ? 63 - __clzll((long long)meta.start) : 0;
-            const uint32_t ph = n & 1;
-
-            // ---- S_dec = diag(P) S_in and D_end as bf16 tiles; rowdot(S_in, D_end) ----
-            {
-                const float* src_s = pl.s_in + (size_t(c) * H + h) * (D * D);
-                const float* src_d = pl.d_end + (size_t(c) * H + h) * (D * D);
-                if (!warp_wait(bProl, ph)) { timed_out = true; break; }
-                if (cin || cout) {
-#pragma unroll 1
-                    for (int rb = 0; rb < 32; rb += 4) {
-                        float4 sv[4], dv4[4];
+            // dg's part past the chunk, when its last segment goes on: rowdot(S_out, D_end) =
+            // [no cut] P rowdot(S_in, D_end) + sum over the last segment's rows s of Ktb_s T2_s
+            float carry = 0.f;
+            if (!warp_wait(bSt, ph)) { timed_out = true; break; }
+            if (cout && fc == C) {
+                float acc = 0.f;
+#pragma unroll 2
+                for (int gi = 0; gi < 16; ++gi) {
+                    const uint32_t off = eoff128(ch, gi * 8);
+                    const uint4 sh = *reinterpret_cast<const uint4*>(sm + kGSH + off);
+                    const uint4 sl = *reinterpret_cast<const uint4*>(sm + kGSL + off);
+                    const uint4 dh = *reinterpret_cast<const uint4*>(sm + kGDH + off);
+                    const uint4 dl = *reinterpret_cast<const uint4*>(sm + kGDL + off);
+                    const uint32_t a4[4] = {sh.x, sh.y, sh.z, sh.w}, b4[4] = {sl.x, sl.y, sl.z, sl.w};
+                    const uint32_t c4[4] = {dh.x, dh.y, dh.z, dh.w}, d4[4] = {dl.x, dl.y, dl.z, dl.w};
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int r = wr * 32 + rb + u;
-                            sv[u] = cin ? __ldcs(reinterpret_cast<const float4*>(src_s + r * D) + lane)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-                            dv4[u] = cout ? __ldcs(reinterpret_cast<const float4*>(src_d + r * D) + lane)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int r = wr * 32 + rb + u;
-                            const uint32_t off = eoff128(r, 4 * lane);
-                            if (cin) {
-                                const float p = s_P[r];
-                                uint2 wh, wl;
-                                split2(p * sv[u].x, p * sv[u].y, wh.x, wl.x);
-                                split2(p * sv[u].z, p * sv[u].w, wh.y, wl.y);
-                                *reinterpret_cast<uint2*>(sm + kGSD + off) = wh;
-                                *reinterpret_cast<uint2*>(sm + kGSDL + off) = wl;
-                            }
-                            if (cout) {
-                                uint2 wh, wl;
-                                split2(dv4[u].x, dv4[u].y, wh.x, wl.x);
-                                split2(dv4[u].z, dv4[u].w, wh.y, wl.y);
-                                *reinterpret_cast<uint2*>(sm + kGDE + off) = wh;
-                                *reinterpret_cast<uint2*>(sm + kGDEL + off) = wl;
-                                if (nocut) {
-                                    float dot = sv[u].x * dv4[u].x + sv[u].y * dv4[u].y +
-                                                sv[u].z * dv4[u].z + sv[u].w * dv4[u].w;
-#pragma unroll
-                                    for (int m = 16; m > 0; m >>= 1)
-                                        dot += __shfl_xor_sync(0xffffffffu, dot, m);
-                                    if (lane == 0) s_rd[r] = dot;
-                                }
-                            }
-                        }
+                    for (int e = 0; e < 4; ++e) {
+                        const float s0 = __uint_as_float(a4[e] << 16) + __uint_as_float(b4[e] << 16);
+                        const float s1 = __uint_as_float(a4[e] & 0xffff0000u) + __uint_as_float(b4[e] & 0xffff0000u);
+                        const float d0 = __uint_as_float(c4[e] << 16) + __uint_as_float(d4[e] << 16);
+                        const float d1 = __uint_as_float(c4[e] & 0xffff0000u) + __uint_as_float(d4[e] & 0xffff0000u);
+                        acc = fmaf(s0, d0, acc);
+                        acc = fmaf(s1, d1, acc);
                     }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bConv);
+                carry = Pch * acc;
             }
-            // ---- A' = scale mask(SC), W = mask(W) as hi/lo tiles (over D_end_lo, once read) ----
+            // A' = scale mask(SC), W = mask(W) as hi/lo tiles, over D_end_lo once it is read
             if (!warp_wait(bScores, ph)) { timed_out = true; break; }
             if (!warp_wait(bStates, ph)) { timed_out = true; break; }
             tc_fence_after();
-            mask_tiles(tl + kTmSC, sm + kGAH, sm + kGAL, meta.start, meta.valid, prm.scale, qd, lane);
-            mask_tiles(tl + kTmW, sm + kGWH, sm + kGWL, meta.start, meta.valid, 1.f, qd, lane);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bMasked);
-
-            // ---- epilogue ----
-            if (!warp_wait(bDone, ph)) { timed_out = true; break; }
-            tc_fence_after();
-            const float scale = prm.scale;
-            // the segment at the chunk's end goes on: dg's part past the chunk,
-            // rowdot(S_out, D_end) = [no cut] P rowdot(S_in, D_end) + sum_s Ktb_s T2_s
-            float carry = 0.f;
             if (cout) {
-                carry = nocut ? s_P[i] * s_rd[i] : 0.f;
 #pragma unroll 1
-                for (int blk = lo_last >> 4; blk < 4; ++blk) {
-                    uint32_t t2[16];
-                    tmem_ld16(tl + kTmT2 + blk * 16, t2);
+                for (int blk = lo_last >> 3; blk < 8; ++blk) {
+                    uint32_t t2[8];
+                    tmem_ld8(tl + kTmT2 + blk * 8, t2);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int s = blk * 16 + j;
+                    for (int j = 0; j < 8; ++j) {
+                        const int s = blk * 8 + j;
                         if (s >= lo_last) {
-                            const uint32_t o = eoff(s, i);
+                            const uint32_t o = eoff(s, ch);
                             const float kt = ld_bf(sm + kGKH, o) + ld_bf(sm + kGKL, o);
                             carry = fmaf(kt, __uint_as_float(t2[j]), carry);
                         }
                     }
                 }
             }
+            // P and the carry are the previous item's until its epilogue has read them
+            if (n > 0 && !warp_wait(bMiscFree, (n - 1) & 1)) { timed_out = true; break; }
+            s_P[ch] = Pch;
+            s_carry[ch] = carry;
+            mask_tiles(tl + kTmSC, sm + kGAH, sm + kGAL, meta.start, meta.valid, prm.scale, qd, lane);
+            mask_tiles(tl + kTmW, sm + kGWH, sm + kGWL, meta.start, meta.valid, 1.f, qd, lane);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bMasked);
+        }
+    } else {
+        // ================= epilogue: tensor memory and L2 only =================
+        const int qd = warp & 3;                 // TMEM lane quarter
+        const int wr = warp - 6;
+        const int i = qd * 32 + lane;            // key channel (dq, dk, dg) / value channel (dv)
+        const uint32_t tl = tmem + (uint32_t(qd * 32) << 16);
+        const float scale = prm.scale;
+        const size_t row_stride = size_t(H) * D;
+        uint32_t n = 0;
+        for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+            const int c = int(item / H), h = int(item % H);
+            const ChunkMeta meta = pl.meta[c];
+            const int fc = pl.first_cut[c];
+            const bool cout = (c + 1 < n_chunks) && pl.first_cut[c + 1] > 0;
+            const int lo_last = meta.start ? 63 - __clzll((long long)meta.start) : 0;
+            const uint32_t ph = n & 1;
+            if (!warp_wait(bMasked, ph)) { timed_out = true; break; }
+            if (!warp_wait(bDone, ph)) { timed_out = true; break; }
+            tc_fence_after();
+            const float Pi = s_P[i];
+            const float carry = s_carry[i];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bMiscFree);
+            const int64_t row0 = int64_t(c) * C;
+            const int t_end = int(prm.N - row0 < C ? prm.N - row0 : C);   // tokens that exist
+            // this thread's element of token t: base + t * H * 128 (32-bit offsets)
+            const size_t ebase = size_t(row0) * row_stride + size_t(h) * D + i;
+            const uint32_t tstride = uint32_t(row_stride);
+            const __nv_bfloat16* qp = prm.q + ebase;
+            const __nv_bfloat16* kp = prm.k + ebase;
+            const __nv_bfloat16* gp = prm.g + ebase;
+            const __nv_bfloat16* bp = prm.beta + size_t(row0) * H + h;
             float run = carry;
             float suf = 0.f;
-            const size_t row_stride = size_t(H) * D;
-#pragma unroll 1
-            for (int blk = 7; blk >= 0; --blk) {
-                // k and g of this thread's channel for the block's 8 tokens (their tiles now
-                // hold S_dec_lo)
-                __nv_bfloat16 kb[8], gb[8];
+            // k, g, q and beta of the block, one block ahead
+            __nv_bfloat16 kn[8], gn[8], qn[8], bn[8];
+            auto fetch = [&](int t0) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const int64_t p = int64_t(c) * C + blk * 8 + j;
-                    const size_t idx = size_t(p < prm.N ? p : 0) * row_stride + size_t(h) * D + i;
-                    kb[j] = prm.k[idx];
-                    gb[j] = prm.g[idx];
+                    const int t = t0 + j;
+                    const __nv_bfloat16 z = __float2bfloat16(0.f);
+                    const bool ok = t < t_end;
+                    kn[j] = ok ? kp[uint32_t(t) * tstride] : z;
+                    gn[j] = ok ? gp[uint32_t(t) * tstride] : z;
+                    qn[j] = ok ? qp[uint32_t(t) * tstride] : z;
+                    bn[j] = ok ? bp[uint32_t(t) * uint32_t(H)] : z;
                 }
+            };
+            fetch(56);
+#pragma unroll 1
+            for (int blk = 7; blk >= 0; --blk) {
+                __nv_bfloat16 kb[8], gb[8], qb[8];
+                float bb[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    kb[j] = kn[j];
+                    gb[j] = gn[j];
+                    qb[j] = qn[j];
+                    bb[j] = ((meta.valid >> (blk * 8 + j)) & 1ull) ? __bfloat162float(bn[j]) : 0.f;
+                }
+                if (blk > 0) fetch((blk - 1) * 8);
                 uint32_t aQ[8], aQs[8], aK[8], aT2[8], aV[8], aVs[8];
                 tmem_ld8(tl + kTmQ + blk * 8, aQ);
                 tmem_ld8(tl + kTmQs + blk * 8, aQs);
@@ -1083,26 +1179,26 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                 tmem_ld8(tl + kTmV + blk * 8, aV);
                 tmem_ld8(tl + kTmVs + blk * 8, aVs);
                 tmem_ld_wait();
+                float db[8];
 #pragma unroll
                 for (int j = 7; j >= 0; --j) {
                     const int t = blk * 8 + j;
-                    const int64_t p = int64_t(c) * C + t;
-                    const uint32_t o = eoff(t, i);
-                    float dq = 0.f, dk = 0.f, dv = 0.f, dg = 0.f, db = 0.f;
+                    float dq = 0.f, dk = 0.f, dv = 0.f, dg = 0.f;
+                    db[j] = 0.f;
                     if ((meta.valid >> t) & 1ull) {
                         const bool carried = t < fc;
                         const bool last = cout && t >= lo_last;
-                        const float qsum = __uint_as_float(aQ[j]) + (carried ? __uint_as_float(aQs[j]) : 0.f);
+                        const float qsum = __uint_as_float(aQ[j]) + (carried ? Pi * __uint_as_float(aQs[j]) : 0.f);
                         const float ksum = scale * __uint_as_float(aK[j]) + (last ? __uint_as_float(aT2[j]) : 0.f);
-                        const float eS = ex2a(suf);
-                        dq = scale * ex2a(-suf) * qsum;
+                        const float eS = ex2a(suf), eN = ex2a(-suf);
+                        dq = scale * eN * qsum;
                         const float dkr = eS * ksum;
-                        dk = s_beta[t] * dkr;
+                        const float kv = __bfloat162float(kb[j]);
+                        dk = bb[j] * dkr;
                         dv = __uint_as_float(aV[j]) + (last ? __uint_as_float(aVs[j]) : 0.f);
-                        db = __bfloat162float(kb[j]) * dkr;
-                        const float qt = ld_bf(sm + kGQH, o) + ld_bf(sm + kGQL, o);
-                        const float kt = ld_bf(sm + kGKH, o) + ld_bf(sm + kGKL, o);
-                        run += scale * qt * qsum - kt * ksum;
+                        db[j] = kv * dkr;
+                        // q dq - k dk = scale Qt qsum - Ktb ksum
+                        run += scale * (__bfloat162float(qb[j]) * eN) * qsum - (bb[j] * kv * eS) * ksum;
                         const bool is_start = (meta.start >> t) & 1ull;
                         dg = is_start ? 0.f : run;
                         if (is_start) run = 0.f;
@@ -1110,32 +1206,29 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                     } else {
                         run = 0.f;
                     }
-                    s_db[t * D + i] = db;
-                    if (p < prm.N) {
-                        const size_t idx = size_t(p) * row_stride + size_t(h) * D + i;
+                    if (t < t_end) {
+                        const size_t idx = ebase + uint32_t(t) * tstride;
                         store_out<To>(prm.dq, idx, dq);
                         store_out<To>(prm.dk, idx, dk);
                         store_out<To>(prm.dv, idx, dv);
                         store_out<To>(prm.dg, idx, dg);
                     }
                 }
+                // dbeta_t = sum over the 128 key channels: this warp's 32, then the 4 warps'
+                // partial sums in a fixed order (the result does not depend on timing)
+                const float part = warp_sum8(db, lane);
+                float* buf = s_dbw + (blk & 1) * 32;
+                if ((lane & 3) == 0) buf[wr * 8 + warp_sum8_entry(lane)] = part;
+                epi_sync();
+                if (wr == 0 && lane < 8) {
+                    const int64_t p = row0 + blk * 8 + lane;
+                    const float sum = ((buf[lane] + buf[8 + lane]) + buf[16 + lane]) + buf[24 + lane];
+                    if (p < prm.N) store_out<To>(prm.dbeta, size_t(p) * H + h, sum);
+                }
             }
             tc_fence_before();
-            epi_sync();
-            // dbeta_t = sum over the 128 key channels, 16 rows per warp
-#pragma unroll 1
-            for (int tt = 0; tt < 16; ++tt) {
-                const int t = wr * 16 + tt;
-                const float4 x = reinterpret_cast<const float4*>(s_db + t * D)[lane];
-                float sum = (x.x + x.y) + (x.z + x.w);
-#pragma unroll
-                for (int m = 16; m > 0; m >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
-                const int64_t p = int64_t(c) * C + t;
-                if (lane == 0 && p < prm.N)
-                    store_out<To>(prm.dbeta, size_t(p) * H + h, sum);
-            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bEmpty);
+            if (lane == 0) mbar_arrive(bTmemFree);
         }
     }
     if (timed_out && lane == 0) set_status(prm.status, KDA_DEV_TIMEOUT);
@@ -1191,6 +1284,7 @@ kda_status_t launch_bwd_tc(const void* q, const void* k, const void* v, const vo
     scan_kernel<true><<<scan_grid, kScanThreads, kScanSmem, stream>>>(m[0], m[2], m[4], sp);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
     GradParams gp;
+    gp.q = static_cast<const __nv_bfloat16*>(q);
     gp.k = static_cast<const __nv_bfloat16*>(k);
     gp.g = static_cast<const __nv_bfloat16*>(g);
     gp.beta = sp.beta;

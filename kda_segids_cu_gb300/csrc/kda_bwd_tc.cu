@@ -45,15 +45,20 @@
 // 0.6x. Accumulation is fp32 in tensor memory.
 //
 // Gradient-kernel tensor-core mapping (kind::f16, transposed outputs: lane = channel, column =
-// token, so that the epilogue's suffix sum over tokens runs within a thread):
+// token, so that the epilogue's suffix sum over tokens runs within a thread). Qt carries the
+// factor scale here (so SC, A' and the dK product include it):
 //   SC    = Qt Ktb^T          M=64  N=64 K=128  A, B K-major                     x3
 //   W     = dO V^T            M=64  N=64 K=128  A, B K-major                     x1
-//   Qs^T  = S_dec dO^T        M=128 N=64 K=128  A K-major (128 rows), B K-major  x2
-//   T2^T  = D_end V^T         M=128 N=64 K=128  A K-major (128 rows), B K-major  x2
-//   Vs^T  = D_end^T Ktb^T     M=128 N=64 K=128  A MN-major, B K-major            x3
-//   dQ^T  = Ktb^T W^T         M=128 N=64 K=64   A MN-major, B K-major            x3
-//   dK^T  = Qt^T W            M=128 N=64 K=64   A MN-major, B MN-major           x3
-//   dV^T  = dO^T A'           M=128 N=64 K=64   A MN-major, B MN-major           x2
+//   Qs^T  = S_in dO^T         M=128 N=64 K=128  A K-major (128 rows), B K-major  x2  -> QQ
+//   T2^T  = D_end V^T         M=128 N=64 K=128  A K-major (128 rows), B K-major  x2  -> KK
+//   Vs^T  = D_end^T Ktb^T     M=128 N=64 K=128  A MN-major, B K-major            x3  -> VV
+//   then the prologue warps scale QQ by P and keep its carried rows, and keep the last
+//   segment's rows of KK and VV, in tensor memory, and the last three accumulate onto them:
+//   dQ^T += Ktb^T W^T         M=128 N=64 K=64   A MN-major, B K-major            x3  -> QQ
+//   dK^T += Qt^T W            M=128 N=64 K=64   A MN-major, B MN-major           x3  -> KK
+//   dV^T += dO^T A'           M=128 N=64 K=64   A MN-major, B MN-major           x2  -> VV
+// QQ, KK and VV are double-buffered, so that an item's products run during the previous item's
+// epilogue.
 // Warp roles (320 threads): 0 TMA producer, 1 MMA issuer, 2-5 prologue (one key channel per
 // thread: Suf, Qt and Ktb), 6-9 the states' conversion, the A' and W tiles and the epilogue.
 // Shared memory holds one item (224 KB of tiles); the lo halves of S_dec and D_end borrow the
@@ -166,23 +171,20 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
     if (status) atomicOr(status, bit);
 }
 
-// 32x32b shape, 16 consecutive columns.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-
 // 32x32b shape, 8 consecutive columns.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                    "=r"(r[6]), "=r"(r[7])
                  : "r"(taddr));
+}
+
+// 32x32b shape, 8 consecutive columns, registers to tensor memory.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+                   "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
 // Barrier 1 among the four epilogue warps only.
@@ -661,8 +663,8 @@ constexpr uint32_t kGDH = kGSH + kTile128;    // D_end_hi
 constexpr uint32_t kGSL = kGK;                // S_in_lo (over k and g)
 constexpr uint32_t kGDL = kGAH;               // D_end_lo (over A' and W)
 constexpr uint32_t kGMisc = kGDH + kTile128;
-// misc: barriers at 0, the TMEM base at 96, beta (float[64], the prologue's) at 128, P
-// (float[128]) at 384, dg's part past the chunk (float[128]) at 896, the epilogue warps'
+// misc: barriers at 0, the TMEM base at 96, beta (float[64], the prologue's) at 128, dg's part
+// past the chunk (float[128]) at 896, the epilogue warps'
 // dbeta partial sums (float[2][4][8], by block parity) at 1408
 constexpr uint32_t kGMiscBytes = 1664;
 constexpr uint32_t kGradSmem = kGMisc + kGMiscBytes + 1024;
@@ -671,12 +673,11 @@ static_assert(kGradSmem <= 232448, "shared memory per CTA");
 // tensor memory (columns)
 constexpr uint32_t kTmSC = 0;      // SC, M=64 layout (row t in lane 32 (t/16) + t%16)
 constexpr uint32_t kTmW = 64;      // W, M=64 layout
-constexpr uint32_t kTmQs = 128;    // Qs^T  (lane = key channel, column = token)
-constexpr uint32_t kTmT2 = 192;    // T2^T  (key channel)
-constexpr uint32_t kTmVs = 256;    // Vs^T  (value channel)
-constexpr uint32_t kTmQ = 320;     // dQ^T  (key channel)
-constexpr uint32_t kTmK = 384;     // dK^T  (key channel)
-constexpr uint32_t kTmV = 448;     // dV^T  (value channel)
+// per buffer b (an item's parity), 192 columns from 128 + 192 b (lane = channel, column = token):
+constexpr uint32_t kTmQQ = 128;    //   QQ: Qs^T, then dQ^T's sum (key channel)
+constexpr uint32_t kTmKK = 192;    //   KK: T2^T, then dK^T's sum (key channel)
+constexpr uint32_t kTmVV = 256;    //   VV: Vs^T, then dV^T's sum (value channel)
+constexpr uint32_t kTmBuf = 192;
 
 struct GradParams {
     const __nv_bfloat16* q;          // read again by the epilogue (from L2)
@@ -804,11 +805,10 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     uint64_t* bStates = bars + 4;    // the products reading S_in and D_end done
     uint64_t* bMasked = bars + 5;    // A' and W tiles, dg's part past the chunk (4 warps)
     uint64_t* bDone = bars + 6;      // all products done: every tile is free
-    uint64_t* bTmemFree = bars + 7;  // the epilogue has read TMEM (4 warps)
-    uint64_t* bMiscFree = bars + 8;  // the epilogue has read P and the carry (4 warps)
+    uint64_t* bTmemFree = bars + 7;  // [2] the epilogue has read the buffer (4 warps)
+    uint64_t* bMiscFree = bars + 9;  // the epilogue has read the carry (4 warps)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 96);
     float* s_beta = reinterpret_cast<float*>(misc + 128);
-    float* s_P = reinterpret_cast<float*>(misc + 384);
     float* s_carry = reinterpret_cast<float*>(misc + 896);
     float* s_dbw = reinterpret_cast<float*>(misc + 1408);
 
@@ -826,7 +826,8 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         mbar_init(bStates, 1);
         mbar_init(bMasked, 4);
         mbar_init(bDone, 1);
-        mbar_init(bTmemFree, 4);
+        mbar_init(&bTmemFree[0], 4);
+        mbar_init(&bTmemFree[1], 4);
         mbar_init(bMiscFree, 4);
         fence_mbar_init();
     }
@@ -953,65 +954,67 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             for (int kk = 0; kk < D / 16; ++kk)
                 mma_bf16(tmem + kTmSC, dQ_L + kofs64(kk), dK_H + kofs64(kk), id64, 1u);
             mma_commit(bScores);
-            // the state products write columns the previous item's epilogue reads
+            // the buffer's previous user is the item two back: its epilogue must have read it
+            const uint32_t tb = tmem + (n & 1) * kTmBuf;
             if (!warp_wait(bSt, ph)) { timed_out = true; break; }
-            if (n > 0 && !warp_wait(bTmemFree, (n - 1) & 1)) { timed_out = true; break; }
+            if (!warp_wait(&bTmemFree[n & 1], ((n >> 1) & 1) ^ 1)) { timed_out = true; break; }
             tc_fence_after();
-            if (cin) {           // Qs^T = S_in dO^T (the decay P is applied in the epilogue)
+            if (cin) {           // QQ = Qs^T = S_in dO^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmQs, dSH + kofs128(kk), dDO + kofs64(kk), idKK, kk > 0 ? 1u : 0u);
+                    mma_bf16(tb + kTmQQ, dSH + kofs128(kk), dDO + kofs64(kk), idKK, kk > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmQs, dSL + kofs128(kk), dDO + kofs64(kk), idKK, 1u);
+                    mma_bf16(tb + kTmQQ, dSL + kofs128(kk), dDO + kofs64(kk), idKK, 1u);
             }
-            if (cout) {          // T2^T = D_end V^T;  Vs^T = D_end^T Ktb^T
+            if (cout) {          // KK = T2^T = D_end V^T;  VV = Vs^T = D_end^T Ktb^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmT2, dDH + kofs128(kk), dV + kofs64(kk), idKK, kk > 0 ? 1u : 0u);
+                    mma_bf16(tb + kTmKK, dDH + kofs128(kk), dV + kofs64(kk), idKK, kk > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmT2, dDL + kofs128(kk), dV + kofs64(kk), idKK, 1u);
+                    mma_bf16(tb + kTmKK, dDL + kofs128(kk), dV + kofs64(kk), idKK, 1u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmVs, mDH + uint64_t(kk * 128), dK_H + kofs64(kk), idMK, kk > 0 ? 1u : 0u);
+                    mma_bf16(tb + kTmVV, mDH + uint64_t(kk * 128), dK_H + kofs64(kk), idMK, kk > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmVs, mDH + uint64_t(kk * 128), dK_L + kofs64(kk), idMK, 1u);
+                    mma_bf16(tb + kTmVV, mDH + uint64_t(kk * 128), dK_L + kofs64(kk), idMK, 1u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tmem + kTmVs, mDL + uint64_t(kk * 128), dK_H + kofs64(kk), idMK, 1u);
+                    mma_bf16(tb + kTmVV, mDL + uint64_t(kk * 128), dK_H + kofs64(kk), idMK, 1u);
             }
             mma_commit(bStates);     // D_end_lo's space is the A' and W tiles'
             if (!warp_wait(bMasked, ph)) { timed_out = true; break; }
             tc_fence_after();
-            // dQ^T = Ktb^T W^T  (K = 64 tokens s; W^T's K-major rows are W's rows)
+            const uint32_t aq = cin ? 1u : 0u, akv = cout ? 1u : 0u;   // onto the state terms
+            // QQ += Ktb^T W^T  (K = 64 tokens s; W^T's K-major rows are W's rows)
 #pragma unroll
             for (int kk = 0; kk < C / 16; ++kk)
-                mma_bf16(tmem + kTmQ, mK_H + uint64_t(kk * 128), dW_H + uint64_t(kk * 2), idMK, kk > 0 ? 1u : 0u);
+                mma_bf16(tb + kTmQQ, mK_H + uint64_t(kk * 128), dW_H + uint64_t(kk * 2), idMK, kk > 0 ? 1u : aq);
 #pragma unroll
             for (int kk = 0; kk < C / 16; ++kk)
-                mma_bf16(tmem + kTmQ, mK_H + uint64_t(kk * 128), dW_L + uint64_t(kk * 2), idMK, 1u);
+                mma_bf16(tb + kTmQQ, mK_H + uint64_t(kk * 128), dW_L + uint64_t(kk * 2), idMK, 1u);
 #pragma unroll
             for (int kk = 0; kk < C / 16; ++kk)
-                mma_bf16(tmem + kTmQ, mK_L + uint64_t(kk * 128), dW_H + uint64_t(kk * 2), idMK, 1u);
-            // dK^T = Qt^T W  (K = 64 tokens t)
+                mma_bf16(tb + kTmQQ, mK_L + uint64_t(kk * 128), dW_H + uint64_t(kk * 2), idMK, 1u);
+            // KK += Qt^T W  (K = 64 tokens t; Qt carries scale)
 #pragma unroll
             for (int kk = 0; kk < C / 16; ++kk)
-                mma_bf16(tmem + kTmK, mQ_H + uint64_t(kk * 128), mW_H + uint64_t(kk * 128), idMM, kk > 0 ? 1u : 0u);
+                mma_bf16(tb + kTmKK, mQ_H + uint64_t(kk * 128), mW_H + uint64_t(kk * 128), idMM, kk > 0 ? 1u : akv);
 #pragma unroll
             for (int kk = 0; kk < C / 16; ++kk)
-                mma_bf16(tmem + kTmK, mQ_H + uint64_t(kk * 128), mW_L + uint64_t(kk * 128), idMM, 1u);
+                mma_bf16(tb + kTmKK, mQ_H + uint64_t(kk * 128), mW_L + uint64_t(kk * 128), idMM, 1u);
 #pragma unroll
             for (int kk = 0; kk < C / 16; ++kk)
-                mma_bf16(tmem + kTmK, mQ_L + uint64_t(kk * 128), mW_H + uint64_t(kk * 128), idMM, 1u);
-            // dV^T = dO^T A'  (K = 64 tokens t)
+                mma_bf16(tb + kTmKK, mQ_L + uint64_t(kk * 128), mW_H + uint64_t(kk * 128), idMM, 1u);
+            // VV += dO^T A'  (K = 64 tokens t)
 #pragma unroll
             for (int kk = 0; kk < C / 16; ++kk)
-                mma_bf16(tmem + kTmV, mDO + uint64_t(kk * 128), mA_H + uint64_t(kk * 128), idMM, kk > 0 ? 1u : 0u);
+                mma_bf16(tb + kTmVV, mDO + uint64_t(kk * 128), mA_H + uint64_t(kk * 128), idMM, kk > 0 ? 1u : akv);
 #pragma unroll
             for (int kk = 0; kk < C / 16; ++kk)
-                mma_bf16(tmem + kTmV, mDO + uint64_t(kk * 128), mA_L + uint64_t(kk * 128), idMM, 1u);
+                mma_bf16(tb + kTmVV, mDO + uint64_t(kk * 128), mA_L + uint64_t(kk * 128), idMM, 1u);
             mma_commit(bDone);
         }
         __syncwarp();
@@ -1036,11 +1039,11 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                 uint32_t qh = 0, ql = 0, kh = 0, kl = 0;
                 if ((meta.valid >> t) & 1ull) {
                     const float qv = ld_bf(sm + kGQL, o), kv = ld_bf(sm + kGK, o);
-                    split1(qv * ex2a(-suf), qh, ql);
+                    split1(prm.scale * qv * ex2a(-suf), qh, ql);
                     split1(kv * s_beta[t] * ex2a(suf), kh, kl);
                     suf += ld_bf(sm + kGG, o) * kLog2e;
                 }
-                st_bf(sm + kGQH, o, qh);
+                    st_bf(sm + kGQH, o, qh);
                 st_bf(sm + kGQL, o, ql);
                 st_bf(sm + kGKH, o, kh);
                 st_bf(sm + kGKL, o, kl);
@@ -1056,9 +1059,10 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             float carry = 0.f;
             if (!warp_wait(bSt, ph)) { timed_out = true; break; }
             if (cout && fc == C) {
-                float acc = 0.f;
-#pragma unroll 2
+                float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
                 for (int gi = 0; gi < 16; ++gi) {
+                    float& acc = acc4[gi & 3];
                     const uint32_t off = eoff128(ch, gi * 8);
                     const uint4 sh = *reinterpret_cast<const uint4*>(sm + kGSH + off);
                     const uint4 sl = *reinterpret_cast<const uint4*>(sm + kGSL + off);
@@ -1076,34 +1080,77 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                         acc = fmaf(s1, d1, acc);
                     }
                 }
-                carry = Pch * acc;
+                carry = Pch * ((acc4[0] + acc4[1]) + (acc4[2] + acc4[3]));
             }
-            // A' = scale mask(SC), W = mask(W) as hi/lo tiles, over D_end_lo once it is read
             if (!warp_wait(bScores, ph)) { timed_out = true; break; }
             if (!warp_wait(bStates, ph)) { timed_out = true; break; }
             tc_fence_after();
+            const uint32_t tb = tl + (n & 1) * kTmBuf;
             if (cout) {
+                float cacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-                for (int blk = lo_last >> 3; blk < 8; ++blk) {
-                    uint32_t t2[8];
-                    tmem_ld8(tl + kTmT2 + blk * 8, t2);
+                for (int hb = lo_last >> 5; hb < 2; ++hb) {
+                    uint32_t t2[32];
+                    tmem_ld32(tb + kTmKK + hb * 32, t2);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int s = blk * 8 + j;
+                    for (int j = 0; j < 32; ++j) {
+                        const int s = hb * 32 + j;
                         if (s >= lo_last) {
                             const uint32_t o = eoff(s, ch);
                             const float kt = ld_bf(sm + kGKH, o) + ld_bf(sm + kGKL, o);
-                            carry = fmaf(kt, __uint_as_float(t2[j]), carry);
+                            cacc[j & 3] = fmaf(kt, __uint_as_float(t2[j]), cacc[j & 3]);
                         }
                     }
                 }
+                carry += (cacc[0] + cacc[1]) + (cacc[2] + cacc[3]);
             }
-            // P and the carry are the previous item's until its epilogue has read them
+            // the state terms, in place, before the products that accumulate onto them: QQ =
+            // P Qs^T on the carried rows (t < fc; S_dec = diag(P) S_in), KK and VV on the last
+            // segment's rows (t >= lo_last), zero elsewhere
+            if (fc > 0) {
+#pragma unroll 1
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + kTmQQ + hb * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        r[j] = (hb * 32 + j < fc) ? __float_as_uint(Pch * __uint_as_float(r[j])) : 0u;
+                    tmem_st32(tb + kTmQQ + hb * 32, r);
+                }
+            }
+            if (cout && lo_last > 0) {
+                const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll 1
+                for (int blk = 0; blk < (lo_last >> 3); ++blk) {
+                    tmem_st8(tb + kTmKK + blk * 8, zero);
+                    tmem_st8(tb + kTmVV + blk * 8, zero);
+                }
+                const int b0 = lo_last & ~7;
+                if (b0 < lo_last) {
+                    uint32_t rk[8], rv[8];
+                    tmem_ld8(tb + kTmKK + b0, rk);
+                    tmem_ld8(tb + kTmVV + b0, rv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (b0 + j < lo_last) {
+                            rk[j] = 0u;
+                            rv[j] = 0u;
+                        }
+                    }
+                    tmem_st8(tb + kTmKK + b0, rk);
+                    tmem_st8(tb + kTmVV + b0, rv);
+                }
+            }
+            tmem_st_wait();
+            // the carry is the previous item's until its epilogue has read it
             if (n > 0 && !warp_wait(bMiscFree, (n - 1) & 1)) { timed_out = true; break; }
-            s_P[ch] = Pch;
             s_carry[ch] = carry;
-            mask_tiles(tl + kTmSC, sm + kGAH, sm + kGAL, meta.start, meta.valid, prm.scale, qd, lane);
+            // A' = mask(SC) (Qt carries scale), W = mask(W) as hi/lo tiles, over D_end_lo once
+            // it is read
+            mask_tiles(tl + kTmSC, sm + kGAH, sm + kGAL, meta.start, meta.valid, 1.f, qd, lane);
             mask_tiles(tl + kTmW, sm + kGWH, sm + kGWL, meta.start, meta.valid, 1.f, qd, lane);
             fence_proxy_async_smem();
             tc_fence_before();
@@ -1122,15 +1169,12 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
             const int c = int(item / H), h = int(item % H);
             const ChunkMeta meta = pl.meta[c];
-            const int fc = pl.first_cut[c];
-            const bool cout = (c + 1 < n_chunks) && pl.first_cut[c + 1] > 0;
-            const int lo_last = meta.start ? 63 - __clzll((long long)meta.start) : 0;
             const uint32_t ph = n & 1;
+            const uint32_t tb = tl + (n & 1) * kTmBuf;
             if (!warp_wait(bMasked, ph)) { timed_out = true; break; }
             if (!warp_wait(bDone, ph)) { timed_out = true; break; }
             tc_fence_after();
-            const float Pi = s_P[i];
-            const float carry = s_carry[i];
+            float run = s_carry[i];              // dg's running sum, from the chunk's end
             __syncwarp();
             if (lane == 0) mbar_arrive(bMiscFree);
             const int64_t row0 = int64_t(c) * C;
@@ -1142,7 +1186,6 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             const __nv_bfloat16* kp = prm.k + ebase;
             const __nv_bfloat16* gp = prm.g + ebase;
             const __nv_bfloat16* bp = prm.beta + size_t(row0) * H + h;
-            float run = carry;
             float suf = 0.f;
             // k, g, q and beta of the block, one block ahead
             __nv_bfloat16 kn[8], gn[8], qn[8], bn[8];
@@ -1171,13 +1214,10 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                     bb[j] = ((meta.valid >> (blk * 8 + j)) & 1ull) ? __bfloat162float(bn[j]) : 0.f;
                 }
                 if (blk > 0) fetch((blk - 1) * 8);
-                uint32_t aQ[8], aQs[8], aK[8], aT2[8], aV[8], aVs[8];
-                tmem_ld8(tl + kTmQ + blk * 8, aQ);
-                tmem_ld8(tl + kTmQs + blk * 8, aQs);
-                tmem_ld8(tl + kTmK + blk * 8, aK);
-                tmem_ld8(tl + kTmT2 + blk * 8, aT2);
-                tmem_ld8(tl + kTmV + blk * 8, aV);
-                tmem_ld8(tl + kTmVs + blk * 8, aVs);
+                uint32_t aQ[8], aK[8], aV[8];
+                tmem_ld8(tb + kTmQQ + blk * 8, aQ);
+                tmem_ld8(tb + kTmKK + blk * 8, aK);
+                tmem_ld8(tb + kTmVV + blk * 8, aV);
                 tmem_ld_wait();
                 float db[8];
 #pragma unroll
@@ -1186,16 +1226,16 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                     float dq = 0.f, dk = 0.f, dv = 0.f, dg = 0.f;
                     db[j] = 0.f;
                     if ((meta.valid >> t) & 1ull) {
-                        const bool carried = t < fc;
-                        const bool last = cout && t >= lo_last;
-                        const float qsum = __uint_as_float(aQ[j]) + (carried ? Pi * __uint_as_float(aQs[j]) : 0.f);
-                        const float ksum = scale * __uint_as_float(aK[j]) + (last ? __uint_as_float(aT2[j]) : 0.f);
+                        // QQ = W Ktb + [carried] P Qs, KK = scale Qt^T W + [last] T2,
+                        // VV = A'^T dO + [last] Vs (the masks and P applied in tensor memory)
+                        const float qsum = __uint_as_float(aQ[j]);
+                        const float ksum = __uint_as_float(aK[j]);
                         const float eS = ex2a(suf), eN = ex2a(-suf);
                         dq = scale * eN * qsum;
                         const float dkr = eS * ksum;
                         const float kv = __bfloat162float(kb[j]);
                         dk = bb[j] * dkr;
-                        dv = __uint_as_float(aV[j]) + (last ? __uint_as_float(aVs[j]) : 0.f);
+                        dv = __uint_as_float(aV[j]);
                         db[j] = kv * dkr;
                         // q dq - k dk = scale Qt qsum - Ktb ksum
                         run += scale * (__bfloat162float(qb[j]) * eN) * qsum - (bb[j] * kv * eS) * ksum;
@@ -1221,14 +1261,14 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                 if ((lane & 3) == 0) buf[wr * 8 + warp_sum8_entry(lane)] = part;
                 epi_sync();
                 if (wr == 0 && lane < 8) {
-                    const int64_t p = row0 + blk * 8 + lane;
+                    const int t = blk * 8 + lane;
                     const float sum = ((buf[lane] + buf[8 + lane]) + buf[16 + lane]) + buf[24 + lane];
-                    if (p < prm.N) store_out<To>(prm.dbeta, size_t(p) * H + h, sum);
+                    if (t < t_end) store_out<To>(prm.dbeta, size_t(row0 + t) * H + h, sum);
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bTmemFree);
+            if (lane == 0) mbar_arrive(&bTmemFree[n & 1]);
         }
     }
     if (timed_out && lane == 0) set_status(prm.status, KDA_DEV_TIMEOUT);

@@ -142,6 +142,39 @@ __device__ __forceinline__ uint32_t bf_bits(float x) {
     return uint32_t(*reinterpret_cast<const uint16_t*>(&b));
 }
 __device__ __forceinline__ float bf_val(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+__device__ __forceinline__ uint32_t ld32(const uint8_t* base, uint32_t off) {
+    return *reinterpret_cast<const uint32_t*>(base + off);
+}
+__device__ __forceinline__ void st32(uint8_t* base, uint32_t off, uint32_t v) {
+    *reinterpret_cast<uint32_t*>(base + off) = v;
+}
+// bf16 pair (even element in the low half) -> fp32 pair, exactly
+__device__ __forceinline__ float2 unpk2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+// packed fp32 pair arithmetic (one f32x2 instruction for two lanes of work)
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 u, v, w;\n\tmov.b64 u, {%2, %3};\n\tmov.b64 v, {%4, %5};\n\t"
+        "mul.rn.f32x2 w, u, v;\n\tmov.b64 {%0, %1}, w;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 u, v, w;\n\tmov.b64 u, {%2, %3};\n\tmov.b64 v, {%4, %5};\n\t"
+        "add.rn.f32x2 w, u, v;\n\tmov.b64 {%0, %1}, w;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 u, v, w, z;\n\tmov.b64 u, {%2, %3};\n\tmov.b64 v, {%4, %5};\n\t"
+        "mov.b64 w, {%6, %7};\n\tfma.rn.f32x2 z, u, v, w;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
 // x = hi + lo, hi = bf16(x), lo = bf16(x - hi)
 __device__ __forceinline__ void split1(float x, uint32_t& hi, uint32_t& lo) {
     hi = bf_bits(x);
@@ -187,8 +220,16 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                  : "memory");
 }
 
-// Barrier 1 among the four epilogue warps only.
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// A barrier among four warps on an mbarrier of count 4 (bounded like every other wait: a
+// warp that gave up elsewhere cannot leave the others waiting for ever). `uses` counts the
+// warp's previous passes, whose parity the wait needs. Returns false on a timeout.
+__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& uses, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+    const bool ok = warp_wait(bar, uses & 1);
+    ++uses;
+    return ok;
+}
 
 // Rows s of t's segment with s <= t (bit s), none when t is padding.
 __device__ __forceinline__ unsigned long long keep_bits(unsigned long long start,
@@ -663,8 +704,9 @@ constexpr uint32_t kGDH = kGSH + kTile128;    // D_end_hi
 constexpr uint32_t kGSL = kGK;                // S_in_lo (over k and g)
 constexpr uint32_t kGDL = kGAH;               // D_end_lo (over A' and W)
 constexpr uint32_t kGMisc = kGDH + kTile128;
-// misc: barriers at 0, the TMEM base at 96, beta (float[64], the prologue's) at 128, dg's part
-// past the chunk (float[128]) at 896, the epilogue warps'
+// misc: barriers at 0, the TMEM base at 96, beta (float[64], the prologue's) at 128, the
+// chunk's base-2 log-decay per key channel (float[128], among the prologue warps) at 384, dg's
+// part past the chunk (float[128]) at 896, the epilogue warps'
 // dbeta partial sums (float[2][4][8], by block parity) at 1408
 constexpr uint32_t kGMiscBytes = 1664;
 constexpr uint32_t kGradSmem = kGMisc + kGMiscBytes + 1024;
@@ -807,8 +849,11 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     uint64_t* bDone = bars + 6;      // all products done: every tile is free
     uint64_t* bTmemFree = bars + 7;  // [2] the epilogue has read the buffer (4 warps)
     uint64_t* bMiscFree = bars + 9;  // the epilogue has read the carry (4 warps)
+    uint64_t* bPSync = bars + 10;    // barrier among the prologue warps
+    uint64_t* bESync = bars + 11;    // barrier among the epilogue warps
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 96);
     float* s_beta = reinterpret_cast<float*>(misc + 128);
+    float* s_P = reinterpret_cast<float*>(misc + 384);
     float* s_carry = reinterpret_cast<float*>(misc + 896);
     float* s_dbw = reinterpret_cast<float*>(misc + 1408);
 
@@ -829,6 +874,8 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         mbar_init(&bTmemFree[0], 4);
         mbar_init(&bTmemFree[1], 4);
         mbar_init(bMiscFree, 4);
+        mbar_init(bPSync, 4);
+        mbar_init(bESync, 4);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -1023,6 +1070,7 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const int qd = warp & 3;                 // TMEM lane quarter
         const int ch = qd * 32 + lane;           // key channel (= TMEM lane of T2)
         const uint32_t tl = tmem + (uint32_t(qd * 32) << 16);
+        uint32_t psync_uses = 0;
         uint32_t n = 0;
         for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
             const int c = int(item / H);
@@ -1032,22 +1080,54 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             const int lo_last = meta.start ? 63 - __clzll((long long)meta.start) : 0;
             const uint32_t ph = n & 1;
             if (!warp_wait(bFull, ph)) { timed_out = true; break; }
-            float suf = 0.f;                       // base-2 log-decay of the real rows after t
+            // Qt and Ktb by channel pairs (2 pm, 2 pm + 1): one thread per pair and half of the
+            // rows, the lower half starting from the sum of g over the upper half's real rows
+            {
+                const int pw = threadIdx.x - 64;
+                const int lower = pw >> 6;               // 0: rows 63..32, 1: rows 31..0
+                const int c0 = 2 * (pw & 63);
+                float2 suf2 = make_float2(0.f, 0.f);
+                if (lower) {
+                    float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
 #pragma unroll 4
-            for (int t = C - 1; t >= 0; --t) {
-                const uint32_t o = eoff(t, ch);
-                uint32_t qh = 0, ql = 0, kh = 0, kl = 0;
-                if ((meta.valid >> t) & 1ull) {
-                    const float qv = ld_bf(sm + kGQL, o), kv = ld_bf(sm + kGK, o);
-                    split1(prm.scale * qv * ex2a(-suf), qh, ql);
-                    split1(kv * s_beta[t] * ex2a(suf), kh, kl);
-                    suf += ld_bf(sm + kGG, o) * kLog2e;
+                    for (int t = 32; t < C; t += 2) {
+                        if ((meta.valid >> t) & 1ull) a = add2(a, unpk2(ld32(sm + kGG, eoff(t, c0))));
+                        if ((meta.valid >> (t + 1)) & 1ull) b = add2(b, unpk2(ld32(sm + kGG, eoff(t + 1, c0))));
+                    }
+                    suf2 = mul2(add2(a, b), make_float2(kLog2e, kLog2e));
                 }
-                    st_bf(sm + kGQH, o, qh);
-                st_bf(sm + kGQL, o, ql);
-                st_bf(sm + kGKH, o, kh);
-                st_bf(sm + kGKL, o, kl);
+                const float2 sc2 = make_float2(prm.scale, prm.scale);
+                const float2 l2e = make_float2(kLog2e, kLog2e);
+                const int t_hi = lower ? 31 : 63;
+#pragma unroll 4
+                for (int t = t_hi; t > t_hi - 32; --t) {
+                    const uint32_t o = eoff(t, c0);
+                    uint32_t qh = 0, ql = 0, kh = 0, kl = 0;
+                    if ((meta.valid >> t) & 1ull) {
+                        const float2 q2 = unpk2(ld32(sm + kGQL, o)), k2 = unpk2(ld32(sm + kGK, o));
+                        const float2 g2 = unpk2(ld32(sm + kGG, o));
+                        const float2 eN = make_float2(ex2a(-suf2.x), ex2a(-suf2.y));
+                        const float2 eS = make_float2(ex2a(suf2.x), ex2a(suf2.y));
+                        const float2 qt = mul2(mul2(q2, sc2), eN);
+                        const float2 kt = mul2(mul2(k2, make_float2(s_beta[t], s_beta[t])), eS);
+                        split2(qt.x, qt.y, qh, ql);
+                        split2(kt.x, kt.y, kh, kl);
+                        suf2 = fma2(g2, l2e, suf2);
+                    }
+                    st32(sm + kGQH, o, qh);
+                    st32(sm + kGQL, o, ql);
+                    st32(sm + kGKH, o, kh);
+                    st32(sm + kGKL, o, kl);
+                }
+                if (lower) {                             // the chunk's whole real g
+                    s_P[c0] = suf2.x;
+                    s_P[c0 + 1] = suf2.y;
+                }
             }
+            if (!group_sync(bPSync, psync_uses, lane)) { timed_out = true; break; }
+            const float suf = s_P[ch];
+            // (the next item rewrites s_P)
+            if (!group_sync(bPSync, psync_uses, lane)) { timed_out = true; break; }
             const bool out_of_range = __any_sync(0xffffffffu, suf < kRangeLog2);
             if (out_of_range && lane == 0) set_status(prm.status, KDA_DEV_DECAY_RANGE);
             const float Pch = ex2a(suf);
@@ -1165,6 +1245,7 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         const uint32_t tl = tmem + (uint32_t(qd * 32) << 16);
         const float scale = prm.scale;
         const size_t row_stride = size_t(H) * D;
+        uint32_t esync_uses = 0;
         uint32_t n = 0;
         for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
             const int c = int(item / H), h = int(item % H);
@@ -1259,13 +1340,14 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                 const float part = warp_sum8(db, lane);
                 float* buf = s_dbw + (blk & 1) * 32;
                 if ((lane & 3) == 0) buf[wr * 8 + warp_sum8_entry(lane)] = part;
-                epi_sync();
+                if (!group_sync(bESync, esync_uses, lane)) { timed_out = true; break; }
                 if (wr == 0 && lane < 8) {
                     const int t = blk * 8 + lane;
                     const float sum = ((buf[lane] + buf[8 + lane]) + buf[16 + lane]) + buf[24 + lane];
                     if (t < t_end) store_out<To>(prm.dbeta, size_t(row0 + t) * H + h, sum);
                 }
             }
+            if (timed_out) break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bTmemFree[n & 1]);

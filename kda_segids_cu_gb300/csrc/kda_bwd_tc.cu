@@ -360,7 +360,7 @@ constexpr uint32_t kSOffG = kTile;          // g -> X_hi
 constexpr uint32_t kSOffY = 2 * kTile;      // y (v or dO), exact
 constexpr uint32_t kSStage = 3 * kTile;
 constexpr uint32_t kSOffMisc = 2 * kSStage;
-// misc: barriers at 0, the TMEM base at 64, per stage s at 128 + 1024 s: the chunk's
+// misc: barriers at 0, the TMEM base at 96, per stage s at 128 + 1024 s: the chunk's
 // descriptor (32 B), beta (float[64]) at +64 and P (float[128]) at +320
 constexpr uint32_t kSMiscStage = 128;
 constexpr uint32_t kScanSmem = kSOffMisc + kSMiscStage + 2 * 1024 + 1024;
@@ -396,7 +396,8 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
     uint64_t* bEmpty = bars + 4;    // [2] the stage's MMAs done
     uint64_t* bReady = bars + 6;    // the state is decayed (4 state warps)
     uint64_t* bSdone = bars + 7;    // the chunk's MMAs done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 64);
+    uint64_t* bPSync = bars + 8;    // barrier among the prologue warps
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 96);
     auto stage_misc = [&](uint32_t s) { return misc + kSMiscStage + s * 1024; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -412,10 +413,11 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
         }
         mbar_init(bReady, 4);
         mbar_init(bSdone, 1);
+        mbar_init(bPSync, 4);
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 128);
+        tmem_alloc(tmem_slot, 256);
         tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
@@ -552,19 +554,27 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
             const uint64_t dXl = sdesc_sw128(st_addr + kSOffX, kPanel, 1024);
             const uint32_t id = idesc_bf16_f32(128, 128, 1, 1);
             const uint32_t acc0 = (f.flags & kFirst) ? 0u : 1u;
+            const uint32_t tS = tmem + (it & 1) * 128;      // this chunk's state buffer
 #pragma unroll
             for (int kk = 0; kk < C / 16; ++kk)
-                mma_bf16(tmem, dY + uint64_t(kk * 128), dXh + uint64_t(kk * 128), id, kk > 0 ? 1u : acc0);
+                mma_bf16(tS, dY + uint64_t(kk * 128), dXh + uint64_t(kk * 128), id, kk > 0 ? 1u : acc0);
 #pragma unroll
             for (int kk = 0; kk < C / 16; ++kk)
-                mma_bf16(tmem, dY + uint64_t(kk * 128), dXl + uint64_t(kk * 128), id, 1u);
+                mma_bf16(tS, dY + uint64_t(kk * 128), dXl + uint64_t(kk * 128), id, 1u);
             mma_commit(bSdone);
             mma_commit(&bEmpty[s]);
         }
         __syncwarp();
     } else if (warp < 6) {
         // ================= prologue: X = x exp(...) as hi/lo, P =================
-        const int ch = threadIdx.x - 64;            // key channel
+        // By channel pairs (2 pm, 2 pm + 1), one thread per pair and half of the rows; the half
+        // that the running sum reaches second starts from the other half's sum of g, read
+        // before either half overwrites g with X_hi.
+        const int pw = threadIdx.x - 64;
+        const int lower = pw >> 6;                  // 0: rows 32..63, 1: rows 0..31
+        const int c0 = 2 * (pw & 63);
+        const float2 l2e = make_float2(kLog2e, kLog2e);
+        uint32_t psync_uses = 0;
         for (uint32_t it = 0;; ++it) {
             const uint32_t s = it & 1, ph = (it >> 1) & 1;
             if (!warp_wait(&bFull[s], ph)) { timed_out = true; break; }
@@ -573,56 +583,100 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
             if (f.flags & kEnd) break;
             uint8_t* st = sm + s * kSStage;
             float* P = reinterpret_cast<float*>(smc + 320);
+            // forward: X_t = beta_t k_t exp(Suf_t) on rows t >= lo, walking down from row 63;
+            // reverse: X_t = scale q_t exp(G_t) on rows t < hi, walking up from row 0
+            float2 run = make_float2(0.f, 0.f);
+            const bool second = kRev ? !lower : lower;   // starts from the other half's sum
+            if (second) {
+                float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
+                const int r0 = kRev ? 0 : 32;
+#pragma unroll 4
+                for (int t = r0; t < r0 + 32; t += 2) {
+                    const bool in0 = kRev ? t < f.hi : t >= f.lo;
+                    const bool in1 = kRev ? t + 1 < f.hi : t + 1 >= f.lo;
+                    if (in0) a = add2(a, unpk2(ld32(st + kSOffG, eoff(t, c0))));
+                    if (in1) b = add2(b, unpk2(ld32(st + kSOffG, eoff(t + 1, c0))));
+                }
+                run = mul2(add2(a, b), l2e);
+            }
+            if (!group_sync(bPSync, psync_uses, lane)) { timed_out = true; break; }
             if (!kRev) {
                 const float* beta = reinterpret_cast<const float*>(smc + 64);
-                float suf = 0.f;                      // base-2 log-decay of the rows after t
+                const int t_hi = lower ? 31 : 63;
 #pragma unroll 4
-                for (int t = C - 1; t >= 0; --t) {
-                    const uint32_t o = eoff(t, ch);
+                for (int t = t_hi; t > t_hi - 32; --t) {
+                    const uint32_t o = eoff(t, c0);
                     uint32_t hi = 0, lo = 0;
                     if (t >= f.lo) {
-                        const float x = ld_bf(st + kSOffX, o) * beta[t] * ex2a(suf);
-                        split1(x, hi, lo);
-                        suf += ld_bf(st + kSOffG, o) * kLog2e;
+                        const float2 x2 = unpk2(ld32(st + kSOffX, o)), g2 = unpk2(ld32(st + kSOffG, o));
+                        const float2 e = make_float2(ex2a(run.x), ex2a(run.y));
+                        const float2 xv = mul2(mul2(x2, make_float2(beta[t], beta[t])), e);
+                        split2(xv.x, xv.y, hi, lo);
+                        run = fma2(g2, l2e, run);
                     }
-                    st_bf(st + kSOffG, o, hi);
-                    st_bf(st + kSOffX, o, lo);
+                    st32(st + kSOffG, o, hi);
+                    st32(st + kSOffX, o, lo);
                 }
-                P[ch] = ex2a(suf);
             } else {
-                float gs = 0.f;                       // base-2 log-decay of rows 0..t
+                const float2 sc2 = make_float2(prm.scale, prm.scale);
+                const int t_lo = lower ? 0 : 32;
 #pragma unroll 4
-                for (int t = 0; t < C; ++t) {
-                    const uint32_t o = eoff(t, ch);
+                for (int t = t_lo; t < t_lo + 32; ++t) {
+                    const uint32_t o = eoff(t, c0);
                     uint32_t hi = 0, lo = 0;
                     if (t < f.hi) {
-                        gs += ld_bf(st + kSOffG, o) * kLog2e;
-                        const float x = prm.scale * ld_bf(st + kSOffX, o) * ex2a(gs);
-                        split1(x, hi, lo);
+                        const float2 x2 = unpk2(ld32(st + kSOffX, o)), g2 = unpk2(ld32(st + kSOffG, o));
+                        run = fma2(g2, l2e, run);
+                        const float2 e = make_float2(ex2a(run.x), ex2a(run.y));
+                        const float2 xv = mul2(mul2(x2, sc2), e);
+                        split2(xv.x, xv.y, hi, lo);
                     }
-                    st_bf(st + kSOffG, o, hi);
-                    st_bf(st + kSOffX, o, lo);
+                    st32(st + kSOffG, o, hi);
+                    st32(st + kSOffX, o, lo);
                 }
-                P[ch] = ex2a(gs);
+            }
+            if (second) {                               // the chunk's whole decay (used when
+                P[c0] = ex2a(run.x);                    // the state goes through the chunk)
+                P[c0 + 1] = ex2a(run.y);
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bProl[s]);
         }
     } else {
-        // ================= state: export, decay =================
+        // ================= state: decay, export =================
+        // The state alternates between two TMEM buffers by chunk: the decay step reads the
+        // previous chunk's buffer and writes this chunk's, which the MMAs then accumulate
+        // into; the export reads the previous buffer after that, while the MMAs run.
         const int qd = warp & 3;                    // TMEM lane quarter
         const int v = qd * 32 + lane;               // value channel (TMEM lane)
         const uint32_t tl = tmem + (uint32_t(qd * 32) << 16);
         uint8_t* const base = reinterpret_cast<uint8_t*>(kRev ? pl.d_end : pl.s_in);
-        // the state as the gradient kernel's operand: hi and lo bf16 tiles, 128 x 128 K-major
-        // 128B-swizzled (row = key channel), element (key, v) at eoff128(key, v)
-        auto put = [&](uint8_t* tile, int key, float x) {
-            uint32_t hi, lo;
-            split1(x, hi, lo);
-            const uint32_t off = eoff128(key, v);
-            *reinterpret_cast<uint16_t*>(tile + off) = uint16_t(hi);
-            *reinterpret_cast<uint16_t*>(tile + kTile128 + off) = uint16_t(lo);
+        // The state as the gradient kernel's operand: hi and lo bf16 tiles, 128 x 128 K-major
+        // 128B-swizzled (row = key channel), element (key, v) at eoff128(key, v). Lanes v, v + 1
+        // swap one value per pair of keys, so that each writes a channel pair of one key (32-bit).
+        const int odd = lane & 1;
+        const int vv = v - odd;                     // the pair's even value channel
+        const uint32_t vbase = uint32_t(vv >> 6) * kPanel128 + uint32_t(vv & 7) * 2;
+        const int vg = (vv >> 3) & 7;
+        auto export_state = [&](uint32_t src, uint8_t* dst) {
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t r[32];
+                tmem_ld32(src + cb * 32, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int jp = 0; jp < 16; ++jp) {
+                    const float x0 = __uint_as_float(r[2 * jp]), x1 = __uint_as_float(r[2 * jp + 1]);
+                    const float recv = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
+                    const int key = cb * 32 + 2 * jp + odd;
+                    const uint32_t off = vbase + uint32_t(key) * 128 + (uint32_t(vg ^ (key & 7)) << 4);
+                    uint32_t hi, lo;
+                    split2(odd ? recv : x0, odd ? x1 : recv, hi, lo);
+                    st32(dst, off, hi);
+                    st32(dst + kTile128, off, lo);
+                }
+            }
         };
         uint32_t nd = 0;                            // MMA completions waited for
         for (uint32_t it = 0;; ++it) {
@@ -631,48 +685,37 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
             uint8_t* smc = stage_misc(s);
             const SDesc f = *reinterpret_cast<const SDesc*>(smc);
             if (f.flags & kEnd) break;
+            const uint32_t cur = tl + (it & 1) * 128, prv = tl + ((it + 1) & 1) * 128;
             if (!(f.flags & kFirst)) {
                 if (!warp_wait(bSdone, nd & 1)) { timed_out = true; break; }
                 ++nd;
                 if (!warp_wait(&bProl[s], ph)) { timed_out = true; break; }
                 tc_fence_after();
                 const float* P = reinterpret_cast<const float*>(smc + 320);
-                uint8_t* dst = base + (size_t(f.slot_pre) * H + f.h) * kStateBytes;
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t r[32];
-                    tmem_ld32(tl + cb * 32, r);
+                    tmem_ld32(prv + cb * 32, r);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float x = __uint_as_float(r[j]);
-                        put(dst, cb * 32 + j, x);
-                        r[j] = __float_as_uint(x * P[cb * 32 + j]);
-                    }
-                    tmem_st32(tl + cb * 32, r);
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * P[cb * 32 + j]);
+                    tmem_st32(cur + cb * 32, r);
                 }
                 tmem_st_wait();
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bReady);
+            if (f.flags & kPre)                     // the state entering this chunk
+                export_state(prv, base + (size_t(f.slot_pre) * H + f.h) * kStateBytes);
             if (f.flags & kLast) {
                 if (!warp_wait(bSdone, nd & 1)) { timed_out = true; break; }
                 ++nd;
                 tc_fence_after();
-                if (f.flags & kPost) {
-                    uint8_t* dst = base + (size_t(f.slot_post) * H + f.h) * kStateBytes;
-#pragma unroll 1
-                    for (int cb = 0; cb < 4; ++cb) {
-                        uint32_t r[32];
-                        tmem_ld32(tl + cb * 32, r);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) put(dst, cb * 32 + j, __uint_as_float(r[j]));
-                    }
-                }
-                tc_fence_before();
+                if (f.flags & kPost)                // the state after the chain's last chunk
+                    export_state(cur, base + (size_t(f.slot_post) * H + f.h) * kStateBytes);
             }
+            tc_fence_before();
         }
     }
     if (timed_out && lane == 0) set_status(prm.status, KDA_DEV_TIMEOUT);
@@ -680,7 +723,7 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 128);
+        tmem_dealloc(tmem, 256);
     }
 }
 

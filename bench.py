@@ -500,9 +500,9 @@ def run_gb300(args):
         dtype=torch.uint8, device=dev)
     bwd_out = None
 
-    def bwd_call():
+    def bwd_call(method="auto"):
         return kda.kda_chunk_bwd_varlen(kin.q, kin.k, kin.v, kin.g, kin.beta, d_o, seg, B=wl.B,
-                                        T=wl.T, workspace=bwd_ws)
+                                        T=wl.T, workspace=bwd_ws, method=method)
 
     bwd_out = bwd_call()
     torch.cuda.synchronize()
@@ -515,6 +515,15 @@ def run_gb300(args):
     bb.record(stream)
     torch.cuda.synchronize()
     bwd_ms = ba.elapsed_time(bb) / n_bwd
+    # the fp32 walks (method "walk"), once, for comparison
+    bwd_walk_ms = None
+    if kin.q.dtype == torch.bfloat16:
+        bwd_out = bwd_call("walk")
+        ba.record(stream)
+        bwd_out = bwd_call("walk")
+        bb.record(stream)
+        torch.cuda.synchronize()
+        bwd_walk_ms = ba.elapsed_time(bb)
     del bwd_out, bwd_ws
 
     # ---- e2e through the public API with host buffers ----
@@ -657,8 +666,11 @@ def run_gb300(args):
                 ("kda_chunk_fwd_varlen", chunk_ms, bytes_launch),
                 ("kda_chunk_fwd_varlen_state", state_ms,
                  bytes_launch + 2 * n_state * H * wl.d_qk * wl.d_v * 4),
-                # reads q, k, g, v, beta, d_o; writes dq, dk, dg, dv, dbeta
+                # reads q, k, g, v, beta, d_o; writes dq, dk, dg, dv, dbeta (the default
+                # method: the tensor-core path for bf16 with 128-wide heads)
                 ("kda_chunk_bwd_varlen", bwd_ms,
+                 N * H * (6 * wl.d_qk + 4 * wl.d_v + 2) * kin.q.element_size()),
+                ("kda_chunk_bwd_varlen (fp32 walks)", bwd_walk_ms,
                  N * H * (6 * wl.d_qk + 4 * wl.d_v + 2) * kin.q.element_size()))
             if ms_ is not None
         },

@@ -528,4 +528,4 @@ __all__ = ["segids_to_cu_seqlens", "short_conv_varlen", "chunk_fwd_varlen",
            "kda_segids_to_cu_seqlens", "kda_short_conv_varlen", "kda_chunk_fwd_varlen",
            "kda_chunk_plan_varlen", "kda_chunk_fwd_varlen_state", "kda_chunk_bwd_varlen", "kda_varlen",
            "chunk_fwd_workspace_bytes", "load_library", "header_functions", "KdaError",
-           "KdaDeviceError", "KDA_DEV_DECAY_RANGE", "KDA_DEV_TIMEOUT"]
+           "KdaDeviceError", "KDA_DEV_DECAY_RANGE", "KDA_DEV_TIMEOUT", "KDA_BWD_AUTO", "KDA_BWD_WALK"]

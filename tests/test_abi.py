@@ -222,3 +222,32 @@ def test_chunk_bwd_rejects_invalid_arguments(lib):
     assert call(gdt=kda.KDA_BF16 + 7) == -1
     assert call(ws=None) == -4
     assert call(ws_bytes=ws - 1) == -4
+
+
+def test_chunk_bwd_ex_rejects_invalid_arguments(lib):
+    """kda_chunk_bwd_varlen_ex: kda_chunk_bwd_varlen's checks, plus the method and the status
+    word's alignment; the workspace size covers either method."""
+    f = lib.kda_chunk_bwd_varlen_ex
+    ws = lib.kda_chunk_bwd_varlen_workspace_size(1, 64, 2, 128, 128, kda.KDA_BF16)
+    # the tensor-core path keeps two fp32-sized states per chunk and head (2 x 64 KB)
+    assert ws >= 2 * 2 * 65536
+    assert lib.kda_chunk_bwd_varlen_workspace_size(1, 64, 2, 128, 128, kda.KDA_F32) < ws
+    args = [FAKE] * 5 + [None, 1, 64, 2, 128, 128, ctypes.c_float(1.0), kda.KDA_BF16, FAKE,
+                         kda.KDA_BF16] + [FAKE] * 5 + [FAKE, ws, kda.KDA_BWD_AUTO, None, None]
+
+    def call(**over):
+        a = list(args)
+        idx = {"q": 0, "B": 6, "dk": 9, "dv": 10, "d_o": 13, "dq": 15, "ws": 20,
+               "ws_bytes": 21, "method": 22, "status": 23}
+        for k, v in over.items():
+            a[idx[k]] = v
+        return f(*a)
+
+    assert call(q=None) == -1
+    assert call(dq=ODD) == -1
+    assert call(method=2) == -1
+    assert call(method=-1) == -1
+    assert call(status=ODD) == -1
+    assert call(dk=96, dv=96) == -2
+    assert call(ws_bytes=ws - 1) == -4
+    assert call(method=kda.KDA_BWD_WALK, ws=None) == -4

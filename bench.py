@@ -108,7 +108,7 @@ def workload_label(wl: synth.Workload) -> str:
 
 def chunk_traffic(wl: synth.Workload):
     import hashlib
-    if wl.name != CHUNK_TRAFFIC["workload"]:
+    if wl.name != CHUNK_TRAFFIC["workload"] or wl != synth.WORKLOADS[wl.name]:
         return None
     h = hashlib.sha1()
     for p in CHUNK_SOURCES:
@@ -259,6 +259,15 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows), "source": "nvidia-smi, 200 ms"}
 
 
+def bench_workload(args) -> synth.Workload:
+    """The workload; --heads keeps its shape and segments with fewer heads, for kernel
+    profiles that must hold little device memory (its line is not the workload's number)."""
+    wl = synth.WORKLOADS[args.workload]
+    if args.heads:
+        wl = dataclasses.replace(wl, H=args.heads)
+    return wl
+
+
 def make_step_inputs(wl: synth.Workload, device):
     """The forward's inputs and the three convs' (x and weights seeded apart), all masked by
     the forward's segment ids, as in one attention layer."""
@@ -276,7 +285,7 @@ def run_gb300(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     maybe_init_dist(ws, "nccl")
-    wl = synth.WORKLOADS[args.workload]
+    wl = bench_workload(args)
     N, H = wl.N, wl.H
     kin, convs = make_step_inputs(wl, dev)
     seg = kin.segment_ids
@@ -500,9 +509,13 @@ def run_gb300(args):
         dtype=torch.uint8, device=dev)
     bwd_out = None
 
+    bwd_status = torch.zeros(1, dtype=torch.int32, device=dev)
+
     def bwd_call(method="auto"):
+        # the status word is read once, after the timing (not after every call)
         return kda.kda_chunk_bwd_varlen(kin.q, kin.k, kin.v, kin.g, kin.beta, d_o, seg, B=wl.B,
-                                        T=wl.T, workspace=bwd_ws, method=method)
+                                        T=wl.T, workspace=bwd_ws, method=method,
+                                        status=bwd_status)
 
     bwd_out = bwd_call()
     torch.cuda.synchronize()
@@ -524,6 +537,8 @@ def run_gb300(args):
         bb.record(stream)
         torch.cuda.synchronize()
         bwd_walk_ms = ba.elapsed_time(bb)
+    if int(bwd_status.item()) != 0:
+        raise RuntimeError(f"kda_chunk_bwd_varlen: device status {int(bwd_status.item()):#x}")
     del bwd_out, bwd_ws
 
     # ---- e2e through the public API with host buffers ----
@@ -739,7 +754,7 @@ def run_reference(args, budget_s: float = 150.0):
         return None
     import oracle
 
-    wl = synth.WORKLOADS[args.workload]
+    wl = bench_workload(args)
     nt = oracle.default_threads()
     seg_np, _ = synth.make_segment_ids(wl, synth.default_seed(wl.name))
     seg = torch.from_numpy(seg_np)
@@ -802,6 +817,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--heads", type=int, default=0,
+                    help="profiling only: the workload with this many heads")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -394,10 +394,10 @@ kda_status_t kda_chunk_bwd_varlen(const void *q, const void *k, const void *v, c
  * epilogue dg and dbeta (dg from its sum within the chunk plus the direct form
  * past it). Operands are bf16 (decayed ones as hi + lo pairs), accumulation
  * fp32, as in the forward kernel, so the gradients hold the bf16 bound of the
- * forward's output (2e-2 RMS per head). As in the forward's whole-chunk form,
- * a chunk whose log-decay on some key channel falls below -80 sets
- * KDA_DEV_DECAY_RANGE and its gradients are unreliable: use KDA_BWD_WALK there.
- * Other inputs take the walks.
+ * forward's output (2e-2 RMS per head). A (chunk, head) whose log-decay on some
+ * key channel falls below -80 is outside the factorised products' range: a last
+ * launch recomputes its gradients by an fp32 token walk over the chunk, from the
+ * stored state and adjoint. Other inputs take the walks.
  */
 kda_status_t kda_chunk_bwd_varlen_ex(const void *q, const void *k, const void *v, const void *g,
                                      const void *beta, const int32_t *segment_ids, int64_t B,

@@ -25,7 +25,7 @@
 //   log-decay G only through G_t - G_s), summed over the tokens whose G g_t enters; the part
 //   past the chunk is the direct form of dg at the next chunk's first token.
 //
-// Three launches after a small planner:
+// Three launches after a small planner, and a last one that is empty unless needed:
 //   scan_kernel<false>  walks each chain of chunks that one segment links (a chunk holding a
 //     start or padding begins a chain) forward in time and stores S_in of every chunk:
 //     S^T (+)= V^T Khat with Khat = beta k exp(Suf) on the rows that reach the chunk's end.
@@ -33,14 +33,16 @@
 //     D^T = D^T diag(P) + dO^T Qhat, Qhat_t = scale q_t exp(G_t) on the rows of the segment the
 //     chunk carries in (G_t = sum of g over the chunk's first t + 1 tokens).
 //   grad_kernel         one (chunk, head) at a time, all gradients (eight MMAs, below).
+//   redo_kernel         the items the gradient kernel listed, in fp32 (below).
 // The scans keep the state in tensor memory (fp32) and export it per chunk; the exponentials
 // there stay within (0, 1], so they need no range check. The gradient kernel's factors
-// exp(-Suf) and exp(Suf) do: a chunk whose log-decay on some channel falls below -80 sets
-// KDA_DEV_DECAY_RANGE (its gradients are then unreliable).
+// exp(-Suf) and exp(Suf) do: a chunk whose log-decay on some channel falls below -80 is
+// listed, and redo_kernel rewrites its gradients by the token recurrence over the chunk,
+// from the stored S_in and D_end.
 //
 // Precision: as in the forward kernel, Qt, Ktb, A' and W are carried as hi + lo bf16 pairs and
-// each product sums the pairs' cross terms; dO and V enter exactly. S_dec and D_end are hi + lo
-// pairs too: rounded once to bf16 (as the forward rounds its S_dec), S_dec alone puts dq's worst
+// each product sums the pairs' cross terms; dO and V enter exactly. S_in and D_end are hi + lo
+// pairs too: rounded once to bf16 (as the forward rounds its S_dec), S_in alone puts dq's worst
 // error at 1.24x the bound on a chunk between two carried ones (fp64 emulation), D_end dk's at
 // 0.6x. Accumulation is fp32 in tensor memory.
 //
@@ -92,19 +94,23 @@ constexpr size_t kStateBytes = size_t(D) * D * 4;
 // ---- workspace ------------------------------------------------------------------------
 
 struct BPlan {
-    int32_t* counters;     // [0] chains, [1] next forward-scan item, [2] next reverse-scan item
+    int32_t* counters;     // [0] chains, [1] next forward-scan item, [2] next reverse-scan item,
+                           // [3] items the gradient kernel left to the fp32 redo
     ChunkMeta* meta;       // [n_chunks] start / real-token masks
     int32_t* first_cut;    // [n_chunks] first start-or-padding row, 64 if none
     int2* chains;          // [n_chunks] (first chunk, chunk after the last)
     int32_t* order;        // [n_chunks] chains, longest first
+    int32_t* redo_flag;    // [n_chunks * H] 1 once the (chunk, head) item is listed in redo
+    int32_t* redo;         // [n_chunks * H] items outside the factorised form's range
     float* s_in;           // [n_chunks][H] state entering the chunk, as hi and lo bf16 tiles
     float* d_end;          // [n_chunks][H] adjoint at the chunk's end, likewise (each 2 x 32 KB:
                            // 128 x 128, row = key channel, K-major 128B-swizzled)
 };
 
-__host__ __device__ inline size_t bplan_bytes(int64_t n_chunks) {
+__host__ __device__ inline size_t bplan_bytes(int64_t n_chunks, int32_t H) {
     return align256(64 * 4) + align256(size_t(n_chunks) * sizeof(ChunkMeta)) +
-           align256(size_t(n_chunks) * 4) * 2 + align256(size_t(n_chunks) * 8);
+           align256(size_t(n_chunks) * 4) * 2 + align256(size_t(n_chunks) * 8) +
+           align256(size_t(n_chunks) * H * 4) * 2;
 }
 
 __host__ __device__ inline BPlan bplan_view(void* ws, int64_t n_chunks, int32_t H) {
@@ -115,6 +121,8 @@ __host__ __device__ inline BPlan bplan_view(void* ws, int64_t n_chunks, int32_t 
     pl.first_cut = reinterpret_cast<int32_t*>(p);  p += align256(size_t(n_chunks) * 4);
     pl.order = reinterpret_cast<int32_t*>(p);      p += align256(size_t(n_chunks) * 4);
     pl.chains = reinterpret_cast<int2*>(p);        p += align256(size_t(n_chunks) * 8);
+    pl.redo_flag = reinterpret_cast<int32_t*>(p);  p += align256(size_t(n_chunks) * H * 4);
+    pl.redo = reinterpret_cast<int32_t*>(p);       p += align256(size_t(n_chunks) * H * 4);
     pl.s_in = reinterpret_cast<float*>(p);         p += size_t(n_chunks) * H * kStateBytes;
     pl.d_end = reinterpret_cast<float*>(p);
     return pl;
@@ -256,8 +264,8 @@ __device__ __forceinline__ uint64_t kofs128(int kk) {
 // start-or-padding row.
 __global__ void __launch_bounds__(256)
 bwd_masks_kernel(const int32_t* __restrict__ seg, int64_t N, RowStartTest row_start,
-                 int64_t n_chunks, void* ws) {
-    BPlan pl = bplan_view(ws, n_chunks, 0);
+                 int64_t n_chunks, int32_t H, void* ws) {
+    BPlan pl = bplan_view(ws, n_chunks, H);
     const int lane = threadIdx.x & 31;
     const int64_t c = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (c >= n_chunks) return;
@@ -278,6 +286,7 @@ bwd_masks_kernel(const int32_t* __restrict__ seg, int64_t N, RowStartTest row_st
         const unsigned long long cut = sm | ~vm;
         pl.first_cut[c] = cut ? (__ffsll((long long)cut) - 1) : C;
     }
+    for (int h = lane; h < H; h += 32) pl.redo_flag[c * H + h] = 0;
 }
 
 constexpr int kChainThreads = 1024;
@@ -314,8 +323,8 @@ __device__ int chain_scan(int v, int* s_warp, int* total) {
 // its end forwards except through the chunk that ends it. Ordered longest first (counting sort,
 // lengths >= 1024 share a bucket). One CTA.
 __global__ void __launch_bounds__(kChainThreads, 1)
-bwd_chains_kernel(int64_t n_chunks, void* ws) {
-    BPlan pl = bplan_view(ws, n_chunks, 0);
+bwd_chains_kernel(int64_t n_chunks, int32_t H, void* ws) {
+    BPlan pl = bplan_view(ws, n_chunks, H);
     __shared__ int s_warp[32];
     __shared__ int s_total;
     __shared__ int hist[kChainThreads];
@@ -349,6 +358,7 @@ bwd_chains_kernel(int64_t n_chunks, void* ws) {
         pl.counters[0] = n;
         pl.counters[1] = 0;
         pl.counters[2] = 0;
+        pl.counters[3] = 0;
     }
 }
 
@@ -1171,8 +1181,11 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
             const float suf = s_P[ch];
             // (the next item rewrites s_P)
             if (!group_sync(bPSync, psync_uses, lane)) { timed_out = true; break; }
+            // a channel whose chunk log-decay is below -80: the factorised products lose it,
+            // so the item goes to the fp32 redo, which rewrites its gradients
             const bool out_of_range = __any_sync(0xffffffffu, suf < kRangeLog2);
-            if (out_of_range && lane == 0) set_status(prm.status, KDA_DEV_DECAY_RANGE);
+            if (out_of_range && lane == 0 && atomicExch(&pl.redo_flag[item], 1) == 0)
+                pl.redo[atomicAdd(&pl.counters[3], 1)] = int32_t(item);
             const float Pch = ex2a(suf);
             fence_proxy_async_smem();
             __syncwarp();
@@ -1405,11 +1418,181 @@ grad_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     }
 }
 
+
+// ---- the fp32 redo of items outside the factorised form's range -------------------------
+// A (chunk, head) item whose chunk log-decay falls below -80 on some key channel is listed
+// by the gradient kernel; this kernel rewrites its gradients with the token recurrence of
+// the chunk in fp32: forward from S_in (the walks' dq_t = scale S_t do_t), then backward
+// from D_end (A_t = scale q_t do_t^T + exp(g_{t+1}) A_{t+1}: dk = beta A v, dv = beta A^T k,
+// dbeta = k^T A v, dg the running sum of q dq - k dk plus rowdot(S_out, D_end) on the last
+// segment). One CTA of 128 threads per item; the states S and A sit in shared memory with
+// rows padded to 129 floats, so that row and column sweeps are both free of bank conflicts.
+// It exits at once when nothing is listed.
+
+constexpr int kRedoThreads = 128;
+constexpr int kRS = D + 1;
+constexpr uint32_t kRedoSmem = uint32_t(2 * D * kRS + C * D + 6 * D + 32) * 4;
+
+struct RedoParams {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const __nv_bfloat16* g;
+    const __nv_bfloat16* beta;
+    const __nv_bfloat16* d_o;
+    float scale;
+    int64_t N;
+    int32_t H;
+    int64_t n_chunks;
+    void* ws;
+    void* dq;
+    void* dk;
+    void* dv;
+    void* dg;
+    void* dbeta;
+};
+
+template <typename To>
+__global__ void __launch_bounds__(kRedoThreads)
+redo_kernel(const __grid_constant__ RedoParams prm) {
+    extern __shared__ float rsm[];
+    float* S = rsm;                     // [128][129] the state (row = key channel)
+    float* A = S + D * kRS;             // [128][129] the adjoint
+    float* dqs = A + D * kRS;           // [64][128] dq of the chunk's rows
+    float* vk = dqs + C * D;            // the current token's k, v, q, dO, g
+    float* vv = vk + D;
+    float* vq = vv + D;
+    float* vo = vq + D;
+    float* vg = vo + D;
+    float* vu = vg + D;                 // (A v) per key channel
+    float* red = vu + D;                // [4] dbeta's partial sums
+    const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
+    const int H = prm.H;
+    BPlan pl = bplan_view(prm.ws, prm.n_chunks, H);
+    const int n = pl.counters[3];
+    const float scale = prm.scale;
+    for (int r = blockIdx.x; r < n; r += gridDim.x) {
+        const int item = pl.redo[r];
+        const int c = item / H, h = item % H;
+        const ChunkMeta meta = pl.meta[c];
+        const bool cin = pl.first_cut[c] > 0;
+        const bool cout = (c + 1 < prm.n_chunks) && pl.first_cut[c + 1] > 0;
+        const int64_t row0 = int64_t(c) * C;
+        const uint8_t* ts = reinterpret_cast<const uint8_t*>(pl.s_in) + (size_t(c) * H + h) * kStateBytes;
+        const uint8_t* td = reinterpret_cast<const uint8_t*>(pl.d_end) + (size_t(c) * H + h) * kStateBytes;
+        auto tok = [&](int t) -> size_t { return (size_t(row0 + t) * H + h) * D; };
+        for (int j = 0; j < D; ++j) {
+            const uint32_t o = eoff128(i, j);
+            S[i * kRS + j] = cin ? ld_bf(ts, o) + ld_bf(ts + kTile128, o) : 0.f;
+        }
+        // forward: S_t and dq_t
+        for (int t = 0; t < C; ++t) {
+            const bool real = (meta.valid >> t) & 1ull;
+            __syncthreads();
+            if (real) {
+                const size_t b = tok(t) + i;
+                vk[i] = __bfloat162float(prm.k[b]);
+                vv[i] = __bfloat162float(prm.v[b]);
+                vo[i] = __bfloat162float(prm.d_o[b]);
+                vg[i] = __bfloat162float(prm.g[b]);
+            }
+            __syncthreads();
+            float dq = 0.f;
+            float* Si = S + i * kRS;
+            if (real) {
+                const bool start = (meta.start >> t) & 1ull;
+                const float e = start ? 0.f : expf(vg[i]);
+                const float bk = __bfloat162float(prm.beta[size_t(row0 + t) * H + h]) * vk[i];
+                float acc = 0.f;
+                for (int j = 0; j < D; ++j) {
+                    const float sv = fmaf(e, Si[j], bk * vv[j]);
+                    Si[j] = sv;
+                    acc = fmaf(sv, vo[j], acc);
+                }
+                dq = scale * acc;
+            } else {
+                for (int j = 0; j < D; ++j) Si[j] = 0.f;
+            }
+            dqs[t * D + i] = dq;
+        }
+        // the adjoint at the chunk's end, and dg's part past the chunk
+        float run = 0.f;
+        {
+            float* Ai = A + i * kRS;
+            const float* Si = S + i * kRS;
+            for (int j = 0; j < D; ++j) {
+                const uint32_t o = eoff128(i, j);
+                const float a = cout ? ld_bf(td, o) + ld_bf(td + kTile128, o) : 0.f;
+                Ai[j] = a;
+                run = fmaf(Si[j], a, run);
+            }
+        }
+        // backward: A_t, dk, dv, dbeta, dg
+        for (int t = C - 1; t >= 0; --t) {
+            const bool real = (meta.valid >> t) & 1ull;
+            const bool start = (meta.start >> t) & 1ull;
+            const float bt = real ? __bfloat162float(prm.beta[size_t(row0 + t) * H + h]) : 0.f;
+            __syncthreads();
+            if (real) {
+                const size_t b = tok(t) + i;
+                vk[i] = __bfloat162float(prm.k[b]);
+                vv[i] = __bfloat162float(prm.v[b]);
+                vq[i] = __bfloat162float(prm.q[b]);
+                vo[i] = __bfloat162float(prm.d_o[b]);
+                vg[i] = __bfloat162float(prm.g[b]);
+            }
+            __syncthreads();
+            float* Ai = A + i * kRS;
+            if (real) {
+                const float sq = scale * vq[i];
+                float u = 0.f;
+                for (int j = 0; j < D; ++j) {
+                    const float a = fmaf(sq, vo[j], Ai[j]);
+                    Ai[j] = a;
+                    u = fmaf(a, vv[j], u);
+                }
+                vu[i] = u;
+            }
+            __syncthreads();
+            float dq = 0.f, dk = 0.f, dv = 0.f, dg = 0.f, dbp = 0.f;
+            if (real) {
+                for (int kk = 0; kk < D; ++kk) dv = fmaf(A[kk * kRS + i], vk[kk], dv);   // column i
+                dv *= bt;
+                dq = dqs[t * D + i];
+                dk = bt * vu[i];
+                dbp = vk[i] * vu[i];
+                run += vq[i] * dq - vk[i] * dk;
+                dg = start ? 0.f : run;
+                if (start) run = 0.f;
+            } else {
+                run = 0.f;
+            }
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) dbp += __shfl_xor_sync(0xffffffffu, dbp, m);
+            if (lane == 0) red[warp] = dbp;
+            if (row0 + t < prm.N) {
+                const size_t b = tok(t) + i;
+                store_out<To>(prm.dq, b, dq);
+                store_out<To>(prm.dk, b, dk);
+                store_out<To>(prm.dv, b, dv);
+                store_out<To>(prm.dg, b, dg);
+            }
+            __syncthreads();
+            if (i == 0 && row0 + t < prm.N)
+                store_out<To>(prm.dbeta, size_t(row0 + t) * H + h, (red[0] + red[1]) + (red[2] + red[3]));
+            // the adjoint handed to row t - 1: exp(g_t) A_t within the segment, else none
+            const float e = (real && !start) ? expf(vg[i]) : 0.f;
+            for (int j = 0; j < D; ++j) Ai[j] *= e;
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace tcb
 
 size_t bwd_tc_workspace_bytes(int64_t N, int32_t H) {
     const int64_t n_chunks = ceil_div(N, kChunk);
-    return tcb::bplan_bytes(n_chunks) + 2 * size_t(n_chunks) * H * tcb::kStateBytes;
+    return tcb::bplan_bytes(n_chunks, H) + 2 * size_t(n_chunks) * H * tcb::kStateBytes;
 }
 
 kda_status_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* g,
@@ -1427,9 +1610,9 @@ kda_status_t launch_bwd_tc(const void* q, const void* k, const void* v, const vo
         return KDA_ERR_CUDA;
     const int sms = max(1, sm_count());
     bwd_masks_kernel<<<unsigned(ceil_div(n_chunks, 8)), 256, 0, stream>>>(
-        seg, N, RowStartTest::make(T_len), n_chunks, ws);
+        seg, N, RowStartTest::make(T_len), n_chunks, H, ws);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-    bwd_chains_kernel<<<1, kChainThreads, 0, stream>>>(n_chunks, ws);
+    bwd_chains_kernel<<<1, kChainThreads, 0, stream>>>(n_chunks, H, ws);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
     if (dynamic_smem_attr<scan_kernel<false>>(int(kScanSmem)) != cudaSuccess ||
         dynamic_smem_attr<scan_kernel<true>>(int(kScanSmem)) != cudaSuccess)
@@ -1473,6 +1656,33 @@ kda_status_t launch_bwd_tc(const void* q, const void* k, const void* v, const vo
             return KDA_ERR_CUDA;
         grad_kernel<__nv_bfloat16><<<grid, kGradThreads, kGradSmem, stream>>>(m[0], m[1], m[2], m[3],
                                                                              m[4], gp);
+    }
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    // the items outside the factorised form's range, if any, in fp32
+    RedoParams rp;
+    rp.q = static_cast<const __nv_bfloat16*>(q);
+    rp.k = gp.k;
+    rp.v = static_cast<const __nv_bfloat16*>(v);
+    rp.g = gp.g;
+    rp.beta = gp.beta;
+    rp.d_o = static_cast<const __nv_bfloat16*>(d_o);
+    rp.scale = scale;
+    rp.N = N;
+    rp.H = H;
+    rp.n_chunks = n_chunks;
+    rp.ws = ws;
+    rp.dq = dq;
+    rp.dk = dk;
+    rp.dv = dv;
+    rp.dg = dg;
+    rp.dbeta = dbeta;
+    if (grad_dtype == KDA_F32) {
+        if (dynamic_smem_attr<redo_kernel<float>>(int(kRedoSmem)) != cudaSuccess) return KDA_ERR_CUDA;
+        redo_kernel<float><<<grid, kRedoThreads, kRedoSmem, stream>>>(rp);
+    } else {
+        if (dynamic_smem_attr<redo_kernel<__nv_bfloat16>>(int(kRedoSmem)) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        redo_kernel<__nv_bfloat16><<<grid, kRedoThreads, kRedoSmem, stream>>>(rp);
     }
     return launch_status();
 }

@@ -135,24 +135,29 @@ def test_full_size_sampled_heads(name):
     _check(grads, ref, inp.segment_ids.cpu(), heads=heads, label=name)
 
 
-def test_strong_decay_sets_the_range_bit():
-    """A chunk whose log-decay falls below -80 on some channel is outside the factorised
-    form's range: the call reports KDA_DEV_DECAY_RANGE (and the walks still hold)."""
-    B, T = 1, 128
+def test_strong_decay_takes_the_fp32_redo():
+    """Chunks whose log-decay falls below -80 on some channel are outside the factorised
+    form's range: the gradient kernel lists them and an fp32 token walk over each such chunk
+    (from the stored S_in and D_end) rewrites their gradients. A segment boundary falls inside
+    the strong chunks, and one head stays in range."""
+    B, T = 2, 64 * 4
     inp = _small_random(B, T, 2, 128, torch.bfloat16, seed=41, max_len=T)
-    g = inp.g.clone()
-    g[:, 0, 5] = -3.0                                 # 64 x -3 = -192 per chunk on one channel
-    inp = synth.KdaInputs(inp.q, inp.k, inp.v, g, inp.beta,
-                          torch.ones(B, T, dtype=torch.int32), [])
+    seg = torch.ones(B, T, dtype=torch.int32)
+    seg[0, 100:] = 2
+    seg[1, 150:200] = 0                               # padding inside a strong chunk
+    seg[1, 200:] = 3
+    g = inp.g.clone().view(B, T, 2, 128)
+    g[0, 64:192, 0, 5] = -3.0                         # 64 x -3 = -192 per chunk, head 0
+    g[1, 128:256, 0, 77] = -2.0
+    inp = synth.KdaInputs(inp.q, inp.k, inp.v, g.view(B * T, 2, 128), inp.beta, seg, [])
     d_o = _d_o(inp.v.shape, 42)
+    ref = _ref(inp, B, T, d_o, scale=0.8)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    _gpu(inp, B, T, d_o, status=status)
-    assert int(status.item()) & kda.KDA_DEV_DECAY_RANGE
-    status.zero_()
-    w = _gpu(inp, B, T, d_o, grad_dtype=torch.float32, method="walk", status=status)
+    got = _gpu(inp, B, T, d_o, scale=0.8, grad_dtype=torch.float32, status=status)
     assert int(status.item()) == 0
-    ref = _ref(inp, B, T, d_o)
-    for name, got, r in zip(NAMES, w, ref):
+    _check(got, ref, seg, label="redo")
+    w = _gpu(inp, B, T, d_o, scale=0.8, grad_dtype=torch.float32, method="walk")
+    for name, gw, r in zip(NAMES, w, ref):
         if name == "dbeta":
-            got, r = got.unsqueeze(-1), r.unsqueeze(-1)
-        check_kda_output(got, r, inp.segment_ids, torch.float32, label=f"walk {name}")
+            gw, r = gw.unsqueeze(-1), r.unsqueeze(-1)
+        check_kda_output(gw, r, seg, torch.float32, label=f"walk {name}")

@@ -93,24 +93,53 @@ constexpr size_t kStateBytes = size_t(D) * D * 4;
 
 // ---- workspace ------------------------------------------------------------------------
 
+// A chain longer than kPiece chunks is cut into pieces of kPiece chunks (in the scan's own
+// order), which run at once: a first pass leaves each piece's end state from a zero start and
+// the product of its chunks' decays in a slot, a combine pass turns those into every piece's
+// true start state, and the export pass starts each piece from it.
+constexpr int kPiece = 16;
+
+__host__ __device__ inline int64_t max_pieces(int64_t n_chunks) { return 2 * n_chunks + 8; }
+__host__ __device__ inline int64_t max_slots(int64_t n_chunks) {
+    return 2 * ((n_chunks + kPiece - 1) / kPiece) + 8;
+}
+constexpr size_t kSlotBytes = size_t(128) * 128 * 4 + 512;   // fp32 state + decay product
+
+struct BDir {                      // one scan direction's work lists
+    int4* pieces;                  // (chain, piece number, pieces in the chain, first slot or -1)
+    int32_t* order;                // pieces, longest first
+    int32_t* pieces_a;             // pieces that leave an end state (all but a chain's last)
+    int4* split;                   // chains cut into pieces: (chain, pieces, first slot, 0)
+    uint8_t* slots;                // [slots][H] kSlotBytes each
+};
+
 struct BPlan {
-    int32_t* counters;     // [0] chains, [1] next forward-scan item, [2] next reverse-scan item,
-                           // [3] items the gradient kernel left to the fp32 redo
+    int32_t* counters;     // [0] chains, [1]/[2] next export-pass item (forward/reverse), [3]
+                           // items the gradient kernel left to the fp32 redo, [4]/[5] pieces,
+                           // [6]/[7] pieces with an end state, [8]/[9] chains cut into pieces,
+                           // [10]/[11] next end-state item, [12]/[13] next combine item
     ChunkMeta* meta;       // [n_chunks] start / real-token masks
     int32_t* first_cut;    // [n_chunks] first start-or-padding row, 64 if none
     int2* chains;          // [n_chunks] (first chunk, chunk after the last)
-    int32_t* order;        // [n_chunks] chains, longest first
+    int32_t* order;        // [n_chunks] (unused)
     int32_t* redo_flag;    // [n_chunks * H] 1 once the (chunk, head) item is listed in redo
     int32_t* redo;         // [n_chunks * H] items outside the factorised form's range
+    BDir dir[2];           // forward, reverse
     float* s_in;           // [n_chunks][H] state entering the chunk, as hi and lo bf16 tiles
     float* d_end;          // [n_chunks][H] adjoint at the chunk's end, likewise (each 2 x 32 KB:
                            // 128 x 128, row = key channel, K-major 128B-swizzled)
 };
 
+__host__ __device__ inline size_t bdir_bytes(int64_t n_chunks, int32_t H) {
+    const size_t np = size_t(max_pieces(n_chunks));
+    return align256(np * 16) + align256(np * 4) * 2 + align256(size_t(n_chunks) * 16) +
+           size_t(max_slots(n_chunks)) * H * kSlotBytes;
+}
+
 __host__ __device__ inline size_t bplan_bytes(int64_t n_chunks, int32_t H) {
     return align256(64 * 4) + align256(size_t(n_chunks) * sizeof(ChunkMeta)) +
            align256(size_t(n_chunks) * 4) * 2 + align256(size_t(n_chunks) * 8) +
-           align256(size_t(n_chunks) * H * 4) * 2;
+           align256(size_t(n_chunks) * H * 4) * 2 + 2 * align256(bdir_bytes(n_chunks, H));
 }
 
 __host__ __device__ inline BPlan bplan_view(void* ws, int64_t n_chunks, int32_t H) {
@@ -123,6 +152,16 @@ __host__ __device__ inline BPlan bplan_view(void* ws, int64_t n_chunks, int32_t 
     pl.chains = reinterpret_cast<int2*>(p);        p += align256(size_t(n_chunks) * 8);
     pl.redo_flag = reinterpret_cast<int32_t*>(p);  p += align256(size_t(n_chunks) * H * 4);
     pl.redo = reinterpret_cast<int32_t*>(p);       p += align256(size_t(n_chunks) * H * 4);
+    for (int d = 0; d < 2; ++d) {
+        uint8_t* q = p;
+        const size_t np = size_t(max_pieces(n_chunks));
+        pl.dir[d].pieces = reinterpret_cast<int4*>(q);  q += align256(np * 16);
+        pl.dir[d].order = reinterpret_cast<int32_t*>(q); q += align256(np * 4);
+        pl.dir[d].pieces_a = reinterpret_cast<int32_t*>(q); q += align256(np * 4);
+        pl.dir[d].split = reinterpret_cast<int4*>(q);   q += align256(size_t(n_chunks) * 16);
+        pl.dir[d].slots = q;
+        p += align256(bdir_bytes(n_chunks, H));
+    }
     pl.s_in = reinterpret_cast<float*>(p);         p += size_t(n_chunks) * H * kStateBytes;
     pl.d_end = reinterpret_cast<float*>(p);
     return pl;
@@ -323,7 +362,7 @@ __device__ int chain_scan(int v, int* s_warp, int* total) {
 // its end forwards except through the chunk that ends it. Ordered longest first (counting sort,
 // lengths >= 1024 share a bucket). One CTA.
 __global__ void __launch_bounds__(kChainThreads, 1)
-bwd_chains_kernel(int64_t n_chunks, int32_t H, void* ws) {
+bwd_chains_kernel(int64_t n_chunks, int32_t H, int32_t split_min, void* ws) {
     BPlan pl = bplan_view(ws, n_chunks, H);
     __shared__ int s_warp[32];
     __shared__ int s_total;
@@ -354,6 +393,83 @@ bwd_chains_kernel(int64_t n_chunks, int32_t H, void* ws) {
     hist[tid] = off;
     __syncthreads();
     for (int k = tid; k < n; k += kChainThreads) pl.order[atomicAdd(&hist[bucket(k)], 1)] = k;
+    __syncthreads();
+    // Pieces, per scan direction. The forward scan runs chunks c_a .. c_b - 1; the reverse one
+    // runs c_from down to c_a + 1, where c_from = c_b when the chain's end chunk carries rows
+    // of its segment (first cut > 0), else c_b - 1. A run of L chunks is one piece when
+    // L <= kPiece, else ceil(L / kPiece) pieces, each but the last with a slot.
+    for (int d = 0; d < 2; ++d) {
+        BDir& bd = pl.dir[d];
+        int p_base = 0, a_base = 0, s_base = 0, x_base = 0;
+        for (int k0 = 0; k0 < n; k0 += kChainThreads) {
+            const int k = k0 + tid;
+            int len = 0;
+            if (k < n) {
+                const int2 ch = pl.chains[k];
+                if (d == 0) {
+                    len = ch.y - ch.x;
+                } else {
+                    const bool head = ch.y < n_chunks && pl.first_cut[ch.y] > 0;
+                    len = (head ? ch.y : ch.y - 1) - ch.x;
+                }
+            }
+            const int np = len <= 0 ? 0 : (len <= split_min ? 1 : (len + kPiece - 1) / kPiece);
+            const int cut = np > 1 ? 1 : 0;
+            const int p_off = chain_scan(np, s_warp, &s_total);
+            const int p_tot = s_total;
+            const int a_off = chain_scan(cut ? np - 1 : 0, s_warp, &s_total);
+            const int a_tot = s_total;
+            const int x_off = chain_scan(cut, s_warp, &s_total);
+            const int x_tot = s_total;
+            const int slot = s_base + a_off;           // one slot per piece but the last
+            for (int j = 0; j < np; ++j) {
+                bd.pieces[p_base + p_off + j] = make_int4(k, j, np, cut ? slot : -1);
+                if (cut && j < np - 1) bd.pieces_a[a_base + a_off + j] = p_base + p_off + j;
+            }
+            if (cut) bd.split[x_base + x_off] = make_int4(k, np, slot, 0);
+            p_base += p_tot;
+            a_base += a_tot;
+            s_base += a_tot;
+            x_base += x_tot;
+            __syncthreads();
+        }
+        // pieces longest first (lengths 1 .. kPiece)
+        auto plen = [&](int i) {
+            const int4 pc = bd.pieces[i];
+            const int2 ch = pl.chains[pc.x];
+            int len;
+            if (d == 0) {
+                len = ch.y - ch.x;
+            } else {
+                const bool head = ch.y < n_chunks && pl.first_cut[ch.y] > 0;
+                len = (head ? ch.y : ch.y - 1) - ch.x;
+            }
+            return pc.z == 1 ? min(len, kPiece) : min(kPiece, len - pc.y * kPiece);
+        };
+        if (tid <= kPiece) hist[tid] = 0;
+        __syncthreads();
+        for (int i = tid; i < p_base; i += kChainThreads) atomicAdd(&hist[kPiece - plen(i)], 1);
+        __syncthreads();
+        if (tid == 0) {
+            int run = 0;
+            for (int b = 0; b <= kPiece; ++b) {
+                const int c = hist[b];
+                hist[b] = run;
+                run += c;
+            }
+        }
+        __syncthreads();
+        for (int i = tid; i < p_base; i += kChainThreads)
+            bd.order[atomicAdd(&hist[kPiece - plen(i)], 1)] = i;
+        __syncthreads();
+        if (tid == 0) {
+            pl.counters[4 + d] = p_base;
+            pl.counters[6 + d] = a_base;
+            pl.counters[8 + d] = x_base;
+            pl.counters[10 + d] = 0;
+            pl.counters[12 + d] = 0;
+        }
+    }
     if (tid == 0) {
         pl.counters[0] = n;
         pl.counters[1] = 0;
@@ -376,10 +492,15 @@ constexpr uint32_t kSMiscStage = 128;
 constexpr uint32_t kScanSmem = kSOffMisc + kSMiscStage + 2 * 1024 + 1024;
 static_assert(2 * kScanSmem <= 232448, "two scan CTAs per SM");
 
-enum : int { kFirst = 1, kLast = 2, kPre = 4, kPost = 8, kEnd = 16 };
+// chunk flags: kFirst the piece starts from zero here; kSeed it starts from its slot's state
+// here (which is exported as this chunk's state); kPre the state entering the chunk is
+// exported; kLast the piece's last chunk; kPost the state after it is exported (the export
+// pass: the chain's next chunk's state; the end-state pass: the piece's end state and decay
+// product, to its slot); kEnd no more work
+enum : int { kFirst = 1, kLast = 2, kPre = 4, kPost = 8, kEnd = 16, kSeed = 32 };
 
 struct SDesc {
-    int c, h, flags, lo, hi, slot_pre, slot_post, pad;
+    int c, h, flags, lo, hi, slot_pre, slot_post, slot_in;
 };
 
 struct ScanParams {
@@ -390,6 +511,7 @@ struct ScanParams {
     int64_t n_chunks;
     void* ws;
     uint32_t* status;
+    int32_t phase;               // 0: the export pass; 1: the end-state pass
 };
 
 // kRev = false: x = k, y = v, exports S_in; kRev = true: x = q, y = dO, exports D_end.
@@ -443,32 +565,42 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
 
     if (warp == 0) {
         // ================= producer =================
-        const int n_items = pl.counters[0] * H;
+        const int dn = kRev ? 1 : 0;
+        const BDir& bd = pl.dir[dn];
+        const bool ends = prm.phase == 1;
+        const int n_items = pl.counters[(ends ? 6 : 4) + dn] * H;
         uint32_t it = 0;
         for (;;) {
             int item = 0;
-            if (lane == 0) item = atomicAdd(&pl.counters[kRev ? 2 : 1], 1);
+            if (lane == 0) item = atomicAdd(&pl.counters[(ends ? 10 : 1) + dn], 1);
             item = __shfl_sync(0xffffffffu, item, 0);
             const bool done = item >= n_items;
             int c_from = 0, cnt = 1, step = 1, h = 0;
             int2 ch = make_int2(0, 0);
+            int4 pc = make_int4(0, 0, 1, -1);
             bool post = false;
             if (!done) {
-                ch = pl.chains[pl.order[item / H]];
+                pc = bd.pieces[ends ? bd.pieces_a[item / H] : bd.order[item / H]];
+                ch = pl.chains[pc.x];
                 h = item % H;
+                // a chain that is not cut is one piece of any length; cut chains run in pieces
+                // of kPiece chunks
                 if (!kRev) {
-                    c_from = ch.x;
-                    cnt = ch.y - ch.x;
+                    c_from = ch.x + pc.y * kPiece;
+                    cnt = pc.z == 1 ? ch.y - c_from : min(kPiece, ch.y - c_from);
                     post = ch.y < n_chunks && pl.first_cut[ch.y] > 0;
                 } else {
                     const bool head = ch.y < n_chunks && pl.first_cut[ch.y] > 0;
-                    c_from = head ? ch.y : ch.y - 1;
-                    cnt = c_from - ch.x;              // chunks c_from down to ch.x + 1
+                    c_from = (head ? ch.y : ch.y - 1) - pc.y * kPiece;
+                    cnt = c_from - ch.x;               // chunks c_from down to ch.x + 1
+                    if (pc.z > 1) cnt = min(kPiece, cnt);
                     step = -1;
                     post = true;
                 }
                 if (cnt <= 0) continue;
             }
+            const bool seeded = !ends && pc.y > 0;     // starts from its slot's state
+            const bool last_piece = pc.y == pc.z - 1;
             for (int k = 0; k < cnt; ++k, ++it) {
                 const uint32_t s = it & 1;
                 const int c = c_from + step * k;
@@ -519,22 +651,24 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
                         SDesc f;
                         f.c = c;
                         f.h = h;
-                        f.flags = (k == 0 ? kFirst : kPre) | (k == cnt - 1 ? kLast : 0) |
-                                  ((k == cnt - 1 && post) ? kPost : 0);
+                        if (k == 0) f.flags = seeded ? (kSeed | kPre) : kFirst;
+                        else f.flags = ends ? 0 : kPre;
+                        if (k == cnt - 1)
+                            f.flags |= kLast | ((ends || (last_piece && post)) ? kPost : 0);
                         if (!kRev) {
                             // the chain's first chunk: only the rows of the segment that reaches
                             // its end (from its last start; none when its last row is padding)
                             const int ls = meta.start ? 63 - __clzll((long long)meta.start) : 0;
-                            f.lo = (k == 0) ? (((meta.valid >> 63) & 1ull) ? ls : C) : 0;
+                            f.lo = (c == ch.x) ? (((meta.valid >> 63) & 1ull) ? ls : C) : 0;
                             f.hi = C;
                         } else {
                             // the chunk that ends the chain: the rows before its first cut
                             f.lo = 0;
-                            f.hi = (k == 0 && c == ch.y) ? fc : C;
+                            f.hi = (c == ch.y) ? fc : C;
                         }
                         f.slot_pre = c;
-                        f.slot_post = kRev ? ch.x : ch.y;
-                        f.pad = 0;
+                        f.slot_post = ends ? pc.w + pc.y : (kRev ? ch.x : ch.y);
+                        f.slot_in = pc.w + pc.y - 1;
                         *d = f;
                     }
                 }
@@ -669,25 +803,36 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
         const int vv = v - odd;                     // the pair's even value channel
         const uint32_t vbase = uint32_t(vv >> 6) * kPanel128 + uint32_t(vv & 7) * 2;
         const int vg = (vv >> 3) & 7;
+        auto export_block = [&](const uint32_t (&r)[32], int cb, uint8_t* dst) {
+#pragma unroll
+            for (int jp = 0; jp < 16; ++jp) {
+                const float x0 = __uint_as_float(r[2 * jp]), x1 = __uint_as_float(r[2 * jp + 1]);
+                const float recv = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
+                const int key = cb * 32 + 2 * jp + odd;
+                const uint32_t off = vbase + uint32_t(key) * 128 + (uint32_t(vg ^ (key & 7)) << 4);
+                uint32_t hi, lo;
+                split2(odd ? recv : x0, odd ? x1 : recv, hi, lo);
+                st32(dst, off, hi);
+                st32(dst + kTile128, off, lo);
+            }
+        };
         auto export_state = [&](uint32_t src, uint8_t* dst) {
 #pragma unroll 1
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t r[32];
                 tmem_ld32(src + cb * 32, r);
                 tmem_ld_wait();
-#pragma unroll
-                for (int jp = 0; jp < 16; ++jp) {
-                    const float x0 = __uint_as_float(r[2 * jp]), x1 = __uint_as_float(r[2 * jp + 1]);
-                    const float recv = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
-                    const int key = cb * 32 + 2 * jp + odd;
-                    const uint32_t off = vbase + uint32_t(key) * 128 + (uint32_t(vg ^ (key & 7)) << 4);
-                    uint32_t hi, lo;
-                    split2(odd ? recv : x0, odd ? x1 : recv, hi, lo);
-                    st32(dst, off, hi);
-                    st32(dst + kTile128, off, lo);
-                }
+                export_block(r, cb, dst);
             }
         };
+        // a piece's slot: its state in fp32 (element (key, v) at key * 128 + v) and, after
+        // it, the product of its chunks' decays per key channel
+        const int dn = kRev ? 1 : 0;
+        auto slot_at = [&](int slot, int h) -> float* {
+            return reinterpret_cast<float*>(pl.dir[dn].slots + (size_t(slot) * H + h) * kSlotBytes);
+        };
+        const bool ends = prm.phase == 1;
+        float pi = 1.f;                             // (end-state pass) decay product, key v
         uint32_t nd = 0;                            // MMA completions waited for
         for (uint32_t it = 0;; ++it) {
             const uint32_t s = it & 1, ph = (it >> 1) & 1;
@@ -696,12 +841,36 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
             const SDesc f = *reinterpret_cast<const SDesc*>(smc);
             if (f.flags & kEnd) break;
             const uint32_t cur = tl + (it & 1) * 128, prv = tl + ((it + 1) & 1) * 128;
-            if (!(f.flags & kFirst)) {
+            const float* P = reinterpret_cast<const float*>(smc + 320);
+            if (f.flags & kFirst) {
+                pi = 1.f;
+                if (ends) {                         // the decay product needs every chunk's P
+                    if (!warp_wait(&bProl[s], ph)) { timed_out = true; break; }
+                    pi *= P[v];
+                }
+            } else if (f.flags & kSeed) {
+                // the piece's true start state, from its slot: exported as this chunk's entering
+                // state, then decayed into this chunk's buffer
+                if (!warp_wait(&bProl[s], ph)) { timed_out = true; break; }
+                const float* src = slot_at(f.slot_in, f.h) + v;
+                uint8_t* dst = base + (size_t(f.slot_pre) * H + f.h) * kStateBytes;
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__ldcg(src + (cb * 32 + j) * D));
+                    export_block(r, cb, dst);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * P[cb * 32 + j]);
+                    tmem_st32(cur + cb * 32, r);
+                }
+                tmem_st_wait();
+            } else {
                 if (!warp_wait(bSdone, nd & 1)) { timed_out = true; break; }
                 ++nd;
                 if (!warp_wait(&bProl[s], ph)) { timed_out = true; break; }
                 tc_fence_after();
-                const float* P = reinterpret_cast<const float*>(smc + 320);
+                if (ends) pi *= P[v];
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t r[32];
@@ -716,14 +885,26 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bReady);
-            if (f.flags & kPre)                     // the state entering this chunk
+            if ((f.flags & kPre) && !(f.flags & kSeed))   // the state entering this chunk
                 export_state(prv, base + (size_t(f.slot_pre) * H + f.h) * kStateBytes);
             if (f.flags & kLast) {
                 if (!warp_wait(bSdone, nd & 1)) { timed_out = true; break; }
                 ++nd;
                 tc_fence_after();
-                if (f.flags & kPost)                // the state after the chain's last chunk
+                if ((f.flags & kPost) && !ends)     // the state after the chain's last chunk
                     export_state(cur, base + (size_t(f.slot_post) * H + f.h) * kStateBytes);
+                if ((f.flags & kPost) && ends) {    // the piece's end state and decay product
+                    float* dst = slot_at(f.slot_post, f.h);
+#pragma unroll 1
+                    for (int cb = 0; cb < 4; ++cb) {
+                        uint32_t r[32];
+                        tmem_ld32(cur + cb * 32, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) __stcg(dst + (cb * 32 + j) * D + v, __uint_as_float(r[j]));
+                    }
+                    dst[D * D + v] = pi;
+                }
             }
             tc_fence_before();
         }
@@ -734,6 +915,66 @@ scan_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ C
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
+    }
+}
+
+
+// The combine pass between the scans' two passes: per chain cut into pieces and head, the true
+// state entering piece j + 1 is T_{j+1} = diag(Pi_j) T_j + E_j (E_j, Pi_j: piece j's end state
+// from a zero start and its decay product; T_0 = 0), written over E_j's slot. Each (chain,
+// head) spreads over kCombineParts CTAs of 256 threads, 8 state elements per thread (element
+// e = key * 128 + v, so key = e >> 7); a step's loads are issued before the previous step's
+// stores, so that the steps' memory round trips overlap.
+constexpr int kCombineParts = 8;
+
+__global__ void __launch_bounds__(256)
+combine_kernel(int64_t n_chunks, int32_t H, int32_t dn, void* ws) {
+    BPlan pl = bplan_view(ws, n_chunks, H);
+    const BDir& bd = pl.dir[dn];
+    const int n = pl.counters[8 + dn] * H * kCombineParts;
+    const int tid = threadIdx.x;
+    for (int item = blockIdx.x; item < n; item += gridDim.x) {
+        const int part = item % kCombineParts;
+        const int ih = item / kCombineParts;
+        const int4 sp = bd.split[ih / H];
+        const int h = ih % H;
+        auto slot = [&](int j) {
+            return reinterpret_cast<float*>(bd.slots + (size_t(sp.z + j) * H + h) * kSlotBytes);
+        };
+        int e[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) e[m] = part * 2048 + tid + 256 * m;
+        float t[8], ev[8], pv[8];
+        const float* e0 = slot(0);                 // T_1 = E_0
+#pragma unroll
+        for (int m = 0; m < 8; ++m) t[m] = __ldcg(e0 + e[m]);
+        if (sp.y > 2) {
+            const float* s1 = slot(1);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                ev[m] = __ldcg(s1 + e[m]);
+                pv[m] = __ldcg(s1 + D * D + (e[m] >> 7));
+            }
+        }
+        for (int j = 1; j < sp.y - 1; ++j) {
+            float en[8], pn[8];
+            if (j + 1 < sp.y - 1) {                // the next step's operands, in flight now
+                const float* sn = slot(j + 1);
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    en[m] = __ldcg(sn + e[m]);
+                    pn[m] = __ldcg(sn + D * D + (e[m] >> 7));
+                }
+            }
+            float* sj = slot(j);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                t[m] = fmaf(pv[m], t[m], ev[m]);
+                __stcg(sj + e[m], t[m]);
+                ev[m] = en[m];
+                pv[m] = pn[m];
+            }
+        }
     }
 }
 
@@ -1612,7 +1853,8 @@ kda_status_t launch_bwd_tc(const void* q, const void* k, const void* v, const vo
     bwd_masks_kernel<<<unsigned(ceil_div(n_chunks, 8)), 256, 0, stream>>>(
         seg, N, RowStartTest::make(T_len), n_chunks, H, ws);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-    bwd_chains_kernel<<<1, kChainThreads, 0, stream>>>(n_chunks, H, ws);
+    // a chain is cut into pieces of kPiece chunks when it is longer than two of them
+    bwd_chains_kernel<<<1, kChainThreads, 0, stream>>>(n_chunks, H, 2 * kPiece, ws);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
     if (dynamic_smem_attr<scan_kernel<false>>(int(kScanSmem)) != cudaSuccess ||
         dynamic_smem_attr<scan_kernel<true>>(int(kScanSmem)) != cudaSuccess)
@@ -1627,10 +1869,22 @@ kda_status_t launch_bwd_tc(const void* q, const void* k, const void* v, const vo
     sp.status = status_dev;
     const int64_t n_items = n_chunks * H;
     const unsigned scan_grid = unsigned(n_items < 2 * sms ? n_items : 2 * sms);
-    scan_kernel<false><<<scan_grid, kScanThreads, kScanSmem, stream>>>(m[1], m[2], m[3], sp);
-    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-    scan_kernel<true><<<scan_grid, kScanThreads, kScanSmem, stream>>>(m[0], m[2], m[4], sp);
-    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    const unsigned comb_grid = unsigned(4 * sms);
+    // each direction: the pieces' end states, the combine, then the export pass
+    for (int dn = 0; dn < 2; ++dn) {
+        for (int phase = 1; phase >= 0; --phase) {
+            sp.phase = phase;
+            if (dn == 0)
+                scan_kernel<false><<<scan_grid, kScanThreads, kScanSmem, stream>>>(m[1], m[2], m[3], sp);
+            else
+                scan_kernel<true><<<scan_grid, kScanThreads, kScanSmem, stream>>>(m[0], m[2], m[4], sp);
+            if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+            if (phase == 1) {
+                combine_kernel<<<comb_grid, 256, 0, stream>>>(n_chunks, H, dn, ws);
+                if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+            }
+        }
+    }
     GradParams gp;
     gp.q = static_cast<const __nv_bfloat16*>(q);
     gp.k = static_cast<const __nv_bfloat16*>(k);

@@ -25,7 +25,9 @@
 //   log-decay G only through G_t - G_s), summed over the tokens whose G g_t enters; the part
 //   past the chunk is the direct form of dg at the next chunk's first token.
 //
-// Three launches after a small planner, and a last one that is empty unless needed:
+// After a small planner (which also cuts chains longer than 32 chunks into 16-chunk pieces,
+// each scan then running as an end-state pass, a combine pass and the export pass), three
+// kernels, and a last one that is empty unless needed:
 //   scan_kernel<false>  walks each chain of chunks that one segment links (a chunk holding a
 //     start or padding begins a chain) forward in time and stores S_in of every chunk:
 //     S^T (+)= V^T Khat with Khat = beta k exp(Suf) on the rows that reach the chunk's end.

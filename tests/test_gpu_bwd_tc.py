@@ -101,6 +101,22 @@ def test_long_segment_and_none():
     assert all(torch.equal(x, y) for x, y in zip(a, b))
 
 
+def test_long_chains_in_pieces():
+    """Chains longer than 32 chunks run in 16-chunk pieces (end states from zero, a combine
+    pass, then the export from the true piece starts): a 70-chunk document, a ragged tail, and
+    a row whose documents end inside chunks, with padding between them."""
+    B, T = 2, 64 * 70 + 13
+    seg = torch.ones(B, T, dtype=torch.int32)
+    seg[1, 2000:2050] = 0
+    seg[1, 2050:4100] = 2
+    seg[1, 4100:] = 3
+    inp = _small_random(B, T, 2, 128, torch.bfloat16, seed=61, max_len=T)
+    inp = synth.KdaInputs(inp.q, inp.k, inp.v, inp.g, inp.beta, seg, [])
+    d_o = _d_o(inp.v.shape, 62)
+    _check(_gpu(inp, B, T, d_o, scale=0.6, grad_dtype=torch.float32),
+           _ref(inp, B, T, d_o, scale=0.6), seg, label="pieces")
+
+
 def test_deterministic_and_agrees_with_walks():
     inp = _small_random(2, 300, 3, 128, torch.bfloat16, seed=31, max_len=120, pad_prob=0.05)
     d_o = _d_o(inp.v.shape, 32)

@@ -48,7 +48,9 @@ constexpr uint32_t kSX = kSW + kTR * kTD * 4;
 constexpr uint32_t kSA = kSX + kTR * kTD * 4;
 constexpr uint32_t kSB = kSA + kTR * kTR * 4;
 constexpr uint32_t kSQ = kSB + kTR * 4;
-constexpr uint32_t kTailSmem = kSQ + 4 * kTD * 4;   // 166,144 B: one CTA per SM
+// and the first 64 rows of an initial state, fetched ahead while its read-out's scores form
+constexpr uint32_t kSS = kSQ + 4 * kTD * 4;
+constexpr uint32_t kTailSmem = kSS + kTR * kTD * 4;  // 198,912 B: one CTA per SM
 
 __device__ __forceinline__ float2 pfma(float2 a, float2 b, float2 c) {
     float2 d;
@@ -97,7 +99,9 @@ struct Tile {                              // shared-memory views of the current
     float* X;
     float* A;
     const float* beta;
-    uint32_t x_addr;                       // shared-state-space address of X
+    const float* S;                        // rows 0..63 of an initial state
+    uint32_t x_addr;                       // shared-state-space addresses of X and S
+    uint32_t s_addr;
 };
 
 // Final state of rows a..e (one segment): out = exp(G_e - G_{a-1}) * base + sum_j Kf_j v_j^T,
@@ -106,25 +110,26 @@ struct Tile {                              // shared-memory views of the current
 __device__ void final_state(const Tile& t, int a, int e, const float* base, float* out) {
     const int tid = threadIdx.x;
     const float* Ge = t.G + e * kTD;
+    const int rg = tid >> 5, cg = tid & 31;        // key rows 8 rg .., value columns 4 cg ..
+    // the base state's block first: its loads are in flight while Kf is formed
+    float4 bx[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        bx[i] = base ? *reinterpret_cast<const float4*>(base + (8 * rg + i) * kTD + 4 * cg)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int idx = tid; idx < (e - a + 1) * kTD; idx += kTailThreads) {
         const int j = a + idx / kTD, c = idx % kTD;
         t.W[j * kTD + c] = t.beta[j] * __bfloat162float(t.k[j * kTD + c]) *
                            expf(Ge[c] - t.G[j * kTD + c]);
     }
     __syncthreads();
-    const int rg = tid >> 5, cg = tid & 31;        // key rows 8 rg .., value columns 4 cg ..
     float2 acc[8][2];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int c = 8 * rg + i;
         const float dec = expf(Ge[c] - (a > 0 ? t.G[(a - 1) * kTD + c] : 0.f));
-        if (base) {
-            const float4 x = *reinterpret_cast<const float4*>(base + c * kTD + 4 * cg);
-            acc[i][0] = make_float2(dec * x.x, dec * x.y);
-            acc[i][1] = make_float2(dec * x.z, dec * x.w);
-        } else {
-            acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
-        }
+        acc[i][0] = make_float2(dec * bx[i].x, dec * bx[i].y);
+        acc[i][1] = make_float2(dec * bx[i].z, dec * bx[i].w);
     }
 #pragma unroll 2
     for (int j = a; j <= e; ++j) {
@@ -157,6 +162,12 @@ __device__ void head_output(const Tile& t, int r, int end, const float* __restri
                             To* o, int64_t p0, int32_t H, int h, float scale) {
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
+    // S0's key rows 0..63 into S now; rows 64..127 go through X once the scores are formed
+#pragma unroll
+    for (int mm = 0; mm < kTR * kTD / 4 / kTailThreads; ++mm) {
+        const int idx = tid + mm * kTailThreads;
+        cp_async16(t.s_addr + idx * 16, S0 + idx * 4, 16);
+    }
     {
         // transposing writes: a warp takes 32 rows x 32 key channels along a diagonal
         // (lane l: row 32 rt + l, channel 32 ct + (l + d) % 32), so that both the row-major
@@ -234,27 +245,28 @@ __device__ void head_output(const Tile& t, int r, int end, const float* __restri
             *reinterpret_cast<float2*>(t.A + jj * kTR + 2 * ta) = make_float2(out[0], out[1]);
         }
     }
-    __syncthreads();                              // X (Kd) is free: S0 goes through it
+    __syncthreads();                              // X (Kd) is free: S0's rows 64.. go through it
     const int tr = tid >> 5, cg = tid & 31;        // rows 4 tr .. +3, value columns 4 cg ..
     const int i0 = 4 * tr;
     const bool mine = i0 + 3 >= r && i0 < end;
     float2 acc[4][2];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int mm = 0; mm < kTR * kTD / 4 / kTailThreads; ++mm) {
+        const int idx = tid + mm * kTailThreads;              // 16-byte group of the 32 KB block
+        cp_async16(t.x_addr + idx * 16, S0 + 64 * kTD + idx * 4, 16);
+    }
+    cp_async_wait_all();
+    __syncthreads();
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {        // Qd^T S0, key rows 64 half .. +63
-#pragma unroll
-        for (int mm = 0; mm < kTR * kTD / 4 / kTailThreads; ++mm) {
-            const int idx = tid + mm * kTailThreads;          // 16-byte group of the 32 KB block
-            cp_async16(t.x_addr + idx * 16, S0 + (64 * half) * kTD + idx * 4, 16);
-        }
-        cp_async_wait_all();
-        __syncthreads();
+        const float* blk = half == 0 ? t.S : t.X;
         if (mine) {
 #pragma unroll 4
             for (int cc = 0; cc < 64; ++cc) {
                 const float4 w = *reinterpret_cast<const float4*>(t.W + (64 * half + cc) * kTR + i0);
-                const float4 sv4 = *reinterpret_cast<const float4*>(t.X + cc * kTD + 4 * cg);
+                const float4 sv4 = *reinterpret_cast<const float4*>(blk + cc * kTD + 4 * cg);
                 const float2 sv[2] = {make_float2(sv4.x, sv4.y), make_float2(sv4.z, sv4.w)};
                 const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -265,8 +277,8 @@ __device__ void head_output(const Tile& t, int r, int end, const float* __restri
                 }
             }
         }
-        __syncthreads();                          // X is read before it is refilled
     }
+    __syncthreads();                              // S and X are read before they are refilled
     if (mine) {
         const int j_hi = (i0 + 4 < end) ? i0 + 4 : end;
         for (int j = r; j < j_hi; ++j) {          // + A V (A is zero outside the segment)
@@ -309,7 +321,9 @@ state_tail_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
     t.X = reinterpret_cast<float*>(sm + kSX);
     t.A = reinterpret_cast<float*>(sm + kSA);
     t.beta = reinterpret_cast<const float*>(sm + kSB);
+    t.S = reinterpret_cast<const float*>(sm + kSS);
     t.x_addr = sbase + kSX;
+    t.s_addr = sbase + kSS;
     const int64_t n_chunks = ceil_div(N, kTR);
     const Plan pl = plan_view(ws, n_chunks);
     const int tid = threadIdx.x;

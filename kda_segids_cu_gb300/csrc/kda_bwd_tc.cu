@@ -123,7 +123,6 @@ struct BPlan {
     ChunkMeta* meta;       // [n_chunks] start / real-token masks
     int32_t* first_cut;    // [n_chunks] first start-or-padding row, 64 if none
     int2* chains;          // [n_chunks] (first chunk, chunk after the last)
-    int32_t* order;        // [n_chunks] (unused)
     int32_t* redo_flag;    // [n_chunks * H] 1 once the (chunk, head) item is listed in redo
     int32_t* redo;         // [n_chunks * H] items outside the factorised form's range
     BDir dir[2];           // forward, reverse
@@ -140,7 +139,7 @@ __host__ __device__ inline size_t bdir_bytes(int64_t n_chunks, int32_t H) {
 
 __host__ __device__ inline size_t bplan_bytes(int64_t n_chunks, int32_t H) {
     return align256(64 * 4) + align256(size_t(n_chunks) * sizeof(ChunkMeta)) +
-           align256(size_t(n_chunks) * 4) * 2 + align256(size_t(n_chunks) * 8) +
+           align256(size_t(n_chunks) * 4) + align256(size_t(n_chunks) * 8) +
            align256(size_t(n_chunks) * H * 4) * 2 + 2 * align256(bdir_bytes(n_chunks, H));
 }
 
@@ -150,7 +149,6 @@ __host__ __device__ inline BPlan bplan_view(void* ws, int64_t n_chunks, int32_t 
     pl.counters = reinterpret_cast<int32_t*>(p);   p += align256(64 * 4);
     pl.meta = reinterpret_cast<ChunkMeta*>(p);     p += align256(size_t(n_chunks) * sizeof(ChunkMeta));
     pl.first_cut = reinterpret_cast<int32_t*>(p);  p += align256(size_t(n_chunks) * 4);
-    pl.order = reinterpret_cast<int32_t*>(p);      p += align256(size_t(n_chunks) * 4);
     pl.chains = reinterpret_cast<int2*>(p);        p += align256(size_t(n_chunks) * 8);
     pl.redo_flag = reinterpret_cast<int32_t*>(p);  p += align256(size_t(n_chunks) * H * 4);
     pl.redo = reinterpret_cast<int32_t*>(p);       p += align256(size_t(n_chunks) * H * 4);
@@ -183,14 +181,6 @@ __device__ __forceinline__ uint32_t eoff128(int r, int ch) {
 __device__ __forceinline__ float ld_bf(const uint8_t* base, uint32_t off) {
     return __uint_as_float(uint32_t(*reinterpret_cast<const uint16_t*>(base + off)) << 16);
 }
-__device__ __forceinline__ void st_bf(uint8_t* base, uint32_t off, uint32_t bits16) {
-    *reinterpret_cast<uint16_t*>(base + off) = uint16_t(bits16);
-}
-__device__ __forceinline__ uint32_t bf_bits(float x) {
-    const __nv_bfloat16 b = __float2bfloat16_rn(x);
-    return uint32_t(*reinterpret_cast<const uint16_t*>(&b));
-}
-__device__ __forceinline__ float bf_val(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 __device__ __forceinline__ uint32_t ld32(const uint8_t* base, uint32_t off) {
     return *reinterpret_cast<const uint32_t*>(base + off);
 }
@@ -224,15 +214,12 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
     return d;
 }
-// x = hi + lo, hi = bf16(x), lo = bf16(x - hi)
-__device__ __forceinline__ void split1(float x, uint32_t& hi, uint32_t& lo) {
-    hi = bf_bits(x);
-    lo = bf_bits(x - bf_val(hi));
-}
+// (a, b) -> a bf16 pair, a in the low half; round to nearest even
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
 }
+// (a, b) = hi + lo as bf16 pairs: hi = bf16 of each, lo = bf16 of the remainder
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
     hi = pack2(a, b);
     lo = pack2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
@@ -361,8 +348,8 @@ __device__ int chain_scan(int v, int* s_warp, int* total) {
 
 // Chains: a chain begins at chunk 0 and at every chunk holding a start or padding, and ends
 // before the next such chunk; no state crosses a chain's first chunk's last cut backwards or
-// its end forwards except through the chunk that ends it. Ordered longest first (counting sort,
-// lengths >= 1024 share a bucket). One CTA.
+// its end forwards except through the chunk that ends it. Each scan direction's chains become
+// pieces, ordered longest first (a counting sort on lengths 1 .. kPiece). One CTA.
 __global__ void __launch_bounds__(kChainThreads, 1)
 bwd_chains_kernel(int64_t n_chunks, int32_t H, int32_t split_min, void* ws) {
     BPlan pl = bplan_view(ws, n_chunks, H);
@@ -382,19 +369,6 @@ bwd_chains_kernel(int64_t n_chunks, int32_t H, int32_t split_min, void* ws) {
     const int n = base;
     for (int k = tid; k < n; k += kChainThreads)
         pl.chains[k].y = (k + 1 < n) ? pl.chains[k + 1].x : int(n_chunks);
-    hist[tid] = 0;
-    __syncthreads();
-    auto bucket = [&](int k) {
-        const int2 ch = pl.chains[k];
-        const int len = min(ch.y - ch.x, kChainThreads);
-        return kChainThreads - len;                  // 0 = longest
-    };
-    for (int k = tid; k < n; k += kChainThreads) atomicAdd(&hist[bucket(k)], 1);
-    __syncthreads();
-    const int off = chain_scan(hist[tid], s_warp, &s_total);
-    hist[tid] = off;
-    __syncthreads();
-    for (int k = tid; k < n; k += kChainThreads) pl.order[atomicAdd(&hist[bucket(k)], 1)] = k;
     __syncthreads();
     // Pieces, per scan direction. The forward scan runs chunks c_a .. c_b - 1; the reverse one
     // runs c_from down to c_a + 1, where c_from = c_b when the chain's end chunk carries rows

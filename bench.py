@@ -261,10 +261,13 @@ class ClockSampler:
 
 def bench_workload(args) -> synth.Workload:
     """The workload; --heads keeps its shape and segments with fewer heads, for kernel
-    profiles that must hold little device memory (its line is not the workload's number)."""
+    profiles that must hold little device memory (its line is not the workload's number);
+    --max-segs changes only the length of cu_seqlens (the no-inflation check)."""
     wl = synth.WORKLOADS[args.workload]
     if args.heads:
         wl = dataclasses.replace(wl, H=args.heads)
+    if args.max_segs:
+        wl = dataclasses.replace(wl, max_segs=args.max_segs)
     return wl
 
 
@@ -735,12 +738,20 @@ def cpu_baseline(wl: synth.Workload, seconds: float = 15.0, seed_heads: int | No
     measured = t_cu + t_conv + t_kda
     t_cu, t_conv, t_kda = t_cu / reps, t_conv / reps, t_kda / reps
     full = t_cu + 3 * t_conv * (wl.F / f) + t_kda * (wl.H / h)
-    return {"value": wl.N / full, "unit": UNIT, "cores": nt, "kind": "oracle",
-            "sample": f"{wl.name}: cu_seqlens in full; 1 conv on {f} of {wl.F} features "
-                      f"(x3 convs, scaled by features); recurrence on {h} of {wl.H} heads "
-                      f"(all {wl.N} tokens, {nt} threads, scaled by heads); "
-                      f"{reps} repetitions, measured {measured:.1f} s",
-            "seconds_full_step_estimate": full}
+    out = {"value": wl.N / full, "unit": UNIT, "cores": nt, "kind": "oracle",
+           "sample": f"{wl.name}: cu_seqlens in full; 1 conv on {f} of {wl.F} features "
+                     f"(x3 convs, scaled by features); recurrence on {h} of {wl.H} heads "
+                     f"(all {wl.N} tokens, {nt} threads, scaled by heads); "
+                     f"{reps} repetitions, measured {measured:.1f} s",
+           "seconds_full_step_estimate": full}
+    if wl.name in ("tiny", "b2"):          # the two small workloads also on one thread
+        t = time.perf_counter()
+        oracle.kda_fwd(kin.q, kin.k, kin.v, kin.g, kin.beta, seg, wl.B, wl.T, n_threads=1)
+        t1 = time.perf_counter() - t
+        out["single_thread"] = {"value": wl.N / (t_cu + 3 * t_conv * (wl.F / f) + t1 * (wl.H / h)),
+                                "unit": UNIT, "cores": 1,
+                                "sample": "the same step, the recurrence on one thread (once)"}
+    return out
 
 
 def run_reference(args, budget_s: float = 150.0):
@@ -819,6 +830,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--heads", type=int, default=0,
                     help="profiling only: the workload with this many heads")
+    ap.add_argument("--max-segs", type=int, default=0,
+                    help="the cu_seqlens length (max_segs + 1) instead of the workload's; the "
+                         "forward does not read cu_seqlens, so only the scan's writes change")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -46,6 +46,7 @@ def test_workloads(name):
     _compare(seg, 1)
     _compare(seg, max(1, wl.max_segs // 7))
     _compare(seg, wl.max_segs * 3 + 1)
+    _compare(seg, 4096)                       # the no-inflation sweep's size
 
 
 def test_random_sweep():
